@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Benchmark of Fibottention's sparse self-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of the workload:
+support build (host), forward (O, LSE) and backward (dQ, dK, dV), through
+the C ABI of libfibatt.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload vitb]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Timing: W untimed steps, then exactly K steps between two CUDA events,
+bracketed by a barrier and torch.cuda.synchronize(); max over ranks.  Inputs
+rotate over enough copies that each step's tensors are evicted from L2 (129
+MB) by the steps in between.  Kernel durations come from CUDA events recorded
+on the launch stream around every fwd and bwd call inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_head_self_gb300 import _native, api  # noqa: E402
+from sparse_head_self_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = ("attended query-key pairs/sec and achieved HBM GB/s (% of GB300 peak), "
+          "fwd and fwd+bwd")
+UNIT = "pairs/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="vitb")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (a timing reduction, not a data path)."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def algorithmic_bytes(wl, backward: bool) -> int:
+    """Minimum HBM bytes of one call: every input row read once, every output
+    row written once (Q,K,V -> O,LSE forward; Q,K,V,O,dO,LSE -> dQ,dK,dV backward)."""
+    e = wl.B * wl.H * wl.N * wl.D
+    s = 4 if wl.dtype == "f32" else 2
+    rows = wl.B * wl.H * wl.N
+    return (8 * e * s + 4 * rows) if backward else (4 * e * s + 4 * rows)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_head_self_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d[workload][kernel]
+        if ent.get("source_hash") != kernel_source_hash():
+            return None
+        return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        if not self.rows:
+            return None
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# --------------------------------------------------------------- gb300 arm
+
+class Step:
+    """Raw C-ABI calls for one step on one rotating buffer set."""
+
+    def __init__(self, wl, dev, rotate: int, seed: int = 0):
+        self.lib = _native.lib()
+        self.wl = wl
+        H = wl.H
+        ab = [api.wythoff_row(i) for i in range(1, H + 1)]
+        w = api.window_schedule(H, wl.w_min, wl.w_max)
+        self.a = (ctypes.c_int64 * H)(*[x[0] for x in ab])
+        self.b = (ctypes.c_int64 * H)(*[x[1] for x in ab])
+        self.w = (ctypes.c_int64 * H)(*w)
+        self.dt = _native.F32 if wl.dtype == "f32" else _native.BF16
+        q, k, v, do = make_inputs(wl, seed)
+        self.host = (q, k, v, do)
+        self.sets = []
+        sup = api.Support.wythoff(H, wl.N, wl.w_min, wl.w_max, wl.diag)
+        self.pairs = sup.total_pairs(wl.B)
+        ws_bytes = sup.bwd_workspace_bytes(wl.B)
+        for r in range(rotate):
+            t = {n: x.to(dev) for n, x in zip(("Q", "K", "V", "dO"), (q, k, v, do))}
+            t["O"] = torch.empty_like(t["Q"])
+            t["LSE"] = torch.empty((wl.B, H, wl.N), dtype=torch.float32, device=dev)
+            for n in ("dQ", "dK", "dV"):
+                t[n] = torch.empty_like(t["Q"])
+            t["ws"] = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+            t["ws_bytes"] = ws_bytes
+            self.sets.append(t)
+        self.ptr = [{n: (x.data_ptr() if isinstance(x, torch.Tensor) else x) for n, x in t.items()}
+                    for t in self.sets]
+
+    def bytes_per_set(self) -> int:
+        t = self.sets[0]
+        return sum(x.numel() * x.element_size() for x in t.values() if isinstance(x, torch.Tensor))
+
+    def run(self, r: int, stream: int, ev=None):
+        L, wl, p = self.lib, self.wl, self.ptr[r]
+        h = ctypes.c_void_p()
+        _native.check(L.fibatt_support_build(wl.H, wl.N, self.a, self.b, self.w, int(wl.diag),
+                                             ctypes.byref(h)))
+        if ev is not None:
+            ev[0].record()
+        _native.check(L.fibatt_fwd(h, wl.B, wl.D, self.dt, p["Q"], p["K"], p["V"], wl.scale, p["O"],
+                                   p["LSE"], stream))
+        if ev is not None:
+            ev[1].record()
+        _native.check(L.fibatt_bwd(h, wl.B, wl.D, self.dt, p["Q"], p["K"], p["V"], p["O"], p["LSE"],
+                                   p["dO"], wl.scale, p["dQ"], p["dK"], p["dV"], p["ws"],
+                                   p["ws_bytes"], stream))
+        if ev is not None:
+            ev[2].record()
+        L.fibatt_support_destroy(h)
+
+
+def run_e2e(step: Step, dev, steps: int):
+    """Same step through the public Python API, with the inputs copied from
+    pinned host memory and every output read back to pinned host memory."""
+    wl = step.wl
+    q, k, v, do = (x.pin_memory() for x in step.host)
+    outs = {n: torch.empty((wl.B, wl.H, wl.N, wl.D), dtype=wl.torch_dtype).pin_memory()
+            for n in ("O", "dQ", "dK", "dV")}
+    outs["LSE"] = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
+    t = step.sets[0]
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do))
+    d2h = sum(x.numel() * x.element_size() for x in outs.values())
+
+    def one():
+        sup = api.Support.wythoff(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag)
+        for n, x in zip(("Q", "K", "V", "dO"), (q, k, v, do)):
+            t[n].copy_(x, non_blocking=True)
+        api.fwd(sup, t["Q"], t["K"], t["V"], wl.scale, O=t["O"], LSE=t["LSE"])
+        api.bwd(sup, t["Q"], t["K"], t["V"], t["O"], t["LSE"], t["dO"], wl.scale, dQ=t["dQ"],
+                dK=t["dK"], dV=t["dV"], workspace=t["ws"])
+        for n in ("O", "LSE", "dQ", "dK", "dV"):
+            outs[n].copy_(t[n], non_blocking=True)
+        sup.close()
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(wl, target_s: float):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of
+    the workload: forward and backward of whole (b, h) heads, all rows."""
+    import oracle
+    cores = oracle.set_threads(oracle.max_threads())
+    q, k, v, do = make_inputs(wl.with_batch(1), 0)
+    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
+    heads = [oracle.Head.fibottention(*oracle.wythoff_row(i + 1), w[i], wl.diag) for i in range(wl.H)]
+    pairs_head = [oracle.support_size(wl.N, hd) if wl.N <= 2048 else
+                  sum(wl.N - abs(int(d)) for d in oracle.signed_table(wl.N, hd)) for hd in heads]
+    done_pairs, done_heads, t0 = 0, 0, time.perf_counter()
+    while True:
+        h = done_heads % wl.H
+        oracle.fwd_head(q[0, h], k[0, h], v[0, h], heads[h], wl.scale)
+        oracle.bwd_head(q[0, h], k[0, h], v[0, h], do[0, h], heads[h], wl.scale)
+        done_pairs += pairs_head[h]
+        done_heads += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or done_heads >= wl.B * wl.H:
+            break
+    return {"value": done_pairs / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"fwd+bwd of {done_heads} of the workload's {wl.B * wl.H} (b,h) heads, "
+                       f"all {wl.N} rows each, fp64, {el:.1f} s")}
+
+
+def gb300_arm(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the gb300 arm")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    wl = WORKLOADS[args.workload]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    probe = Step(wl, dev, 1)
+    per_set = probe.bytes_per_set()
+    rotate = max(2, math.ceil(3 * l2 / per_set) + 1)
+    del probe
+    step = Step(wl, dev, rotate)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    for i in range(args.warmup):
+        step.run(i % rotate, sptr)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    launches0 = step.lib.fibatt_launch_count()
+    start.record()
+    for i in range(K):
+        step.run(i % rotate, sptr, evs[i])
+    end.record()
+    torch.cuda.synchronize(dev)
+    launches = step.lib.fibatt_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    ms_step = elapsed_ms / K
+    value = world * step.pairs * K / (elapsed_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    fb, bb = algorithmic_bytes(wl, False), algorithmic_bytes(wl, True)
+    fwd_gbs, bwd_gbs = fb / fwd_ms / 1e6, bb / bwd_ms / 1e6
+    dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    d_bytes, d_ms = (bb, bwd_ms) if dominant == "bwd" else (fb, fwd_ms)
+    kname = f"fibatt_{dominant}"
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(d_bytes / d_ms / 1e6, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(d_bytes / d_ms / 1e6 / peak, 4),
+                "traffic": recorded_traffic(kname, wl.name),
+                "algorithmic_bytes": d_bytes, "avg_ms": round(d_ms, 5)}
+
+    e2e_ms, h2d, d2h = run_e2e(step, dev, args.e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": (f"{wl.name}: B={wl.B} H={wl.H} N={wl.N} d={wl.D} {wl.dtype}, "
+                                f"Wythoff rows 1..{wl.H}, w {wl.w_min}..{wl.w_max}, "
+                                f"diag={'on' if wl.diag else 'off'}"),
+                   "B_per_gpu": wl.B, "H": wl.H, "N": wl.N,
+                   "step": "support build + fwd + bwd (all hot-path rows)",
+                   "pairs_per_step_per_gpu": step.pairs,
+                   "l2": (f"{rotate} rotating input/output sets of {per_set / 1e6:.0f} MB "
+                          f"(> {l2 / 1e6:.0f} MB L2 between reuses)"),
+                   "parallelism": f"replicas over B, {world} GPU(s), no collective"},
+        "fwd": {"ms": round(fwd_ms, 5), "pairs_per_s": world * step.pairs / (fwd_ms / 1e3),
+                "GB_s": round(fwd_gbs, 1), "frac_hbm": round(fwd_gbs / peak, 4),
+                "algorithmic_bytes": fb},
+        "bwd": {"ms": round(bwd_ms, 5), "pairs_per_s": world * step.pairs / (bwd_ms / 1e3),
+                "GB_s": round(bwd_gbs, 1), "frac_hbm": round(bwd_gbs / peak, 4),
+                "algorithmic_bytes": bb},
+        "fwd_bwd": {"ms": round(fwd_ms + bwd_ms, 5),
+                    "GB_s": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6, 1),
+                    "frac_hbm": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6 / peak, 4)},
+        "roofline": roofline,
+        "e2e": {"value": world * step.pairs / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": args.e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------- reference arm
+
+def reference_arm(args):
+    """The fp64 oracle, as it stands, timed on host cores: each step is a
+    bounded sample (a block of query/key rows of one (b, h) head, forward and
+    backward), sized so that the whole run ends within a few minutes."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = WORKLOADS[args.workload]
+    cores = oracle.set_threads(oracle.max_threads())
+    q, k, v, do = make_inputs(wl.with_batch(1), 0)
+    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
+    heads = [oracle.Head.fibottention(*oracle.wythoff_row(i + 1), w[i], wl.diag) for i in range(wl.H)]
+    tables = [oracle.signed_table(wl.N, hd) for hd in heads]
+
+    def row_pairs(h, rows):
+        return sum(1 for j in rows for d in tables[h] if 0 <= j + int(d) < wl.N)
+
+    def one(i, nrows):
+        h = i % wl.H
+        r0 = (i * nrows) % wl.N
+        rows = [(r0 + t) % wl.N for t in range(nrows)]
+        oracle.fwd_head(q[0, h], k[0, h], v[0, h], heads[h], wl.scale, rows=rows)
+        oracle.bwd_head(q[0, h], k[0, h], v[0, h], do[0, h], heads[h], wl.scale, qrows=rows, krows=rows)
+        return row_pairs(h, rows)
+
+    # size a step so that warmup + steps take about 120 s
+    t0 = time.perf_counter()
+    one(0, 4)
+    per_row = max((time.perf_counter() - t0) / 4, 1e-6)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(1, min(wl.N, budget / per_row)))
+    for i in range(args.warmup):
+        one(i, nrows)
+    pairs, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        pairs += one(i, nrows)
+    el = time.perf_counter() - t0
+    value = pairs / el
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": wl.name, "B_per_gpu": wl.B, "H": wl.H, "N": wl.N,
+                      "step": f"fwd+bwd of {nrows} query/key rows of one (b,h) head"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"{nrows} rows of one head per step, fp64 C oracle"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gb300_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,73 @@
+// Device helpers shared by the libfibatt kernels: row-slice loads/stores
+// between global memory and fp32 registers for the two I/O dtypes.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fibatt {
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// bf16 -> fp32 is exact: the 16 bits are the high half of the fp32 pattern.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two fp32 -> packed bf16x2, round to nearest even (lo at the lower address).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Load 16 consecutive elements (16-byte aligned) as fp32.
+__device__ __forceinline__ void load16(const float *p, float (&x)[16]) {
+    const float4 *v = reinterpret_cast<const float4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float4 t = __ldg(v + i);
+        x[4 * i + 0] = t.x;
+        x[4 * i + 1] = t.y;
+        x[4 * i + 2] = t.z;
+        x[4 * i + 3] = t.w;
+    }
+}
+
+__device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&x)[16]) {
+    const uint4 *v = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint4 t = __ldg(v + i);
+        x[8 * i + 0] = bf16_lo(t.x);
+        x[8 * i + 1] = bf16_hi(t.x);
+        x[8 * i + 2] = bf16_lo(t.y);
+        x[8 * i + 3] = bf16_hi(t.y);
+        x[8 * i + 4] = bf16_lo(t.z);
+        x[8 * i + 5] = bf16_hi(t.z);
+        x[8 * i + 6] = bf16_lo(t.w);
+        x[8 * i + 7] = bf16_hi(t.w);
+    }
+}
+
+__device__ __forceinline__ void store16(float *p, const float (&x)[16]) {
+    float4 *v = reinterpret_cast<float4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+}
+
+__device__ __forceinline__ void store16(__nv_bfloat16 *p, const float (&x)[16]) {
+    uint4 *v = reinterpret_cast<uint4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint4 t;
+        t.x = pack_bf16x2(x[8 * i + 0], x[8 * i + 1]);
+        t.y = pack_bf16x2(x[8 * i + 2], x[8 * i + 3]);
+        t.z = pack_bf16x2(x[8 * i + 4], x[8 * i + 5]);
+        t.w = pack_bf16x2(x[8 * i + 6], x[8 * i + 7]);
+        v[i] = t;
+    }
+}
+
+}  // namespace fibatt

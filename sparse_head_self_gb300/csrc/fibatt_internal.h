@@ -1,0 +1,72 @@
+// Internal declarations shared by the host API and the kernel launchers of
+// libfibatt.  Not part of the public ABI (see include/fibatt.h).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime_api.h>
+
+#include "../../include/fibatt.h"
+
+namespace fibatt {
+
+constexpr int kHeadDim = FIBATT_HEAD_DIM;
+constexpr int kMaxHeads = FIBATT_MAX_HEADS;
+constexpr int kMaxEntries = FIBATT_MAX_ENTRIES;
+
+// Signed-offset tables of every head, passed to kernels by value as a
+// __grid_constant__ argument (a few KB; no device allocation, valid on any
+// device and inside CUDA graphs).  Head h owns entries [start[h], start[h+1])
+// of `off`, ascending.  Query j of head h attends key j + off[t] whenever
+// 0 <= j + off[t] < N.
+struct TableArg {
+    int32_t H;
+    int32_t N;
+    int32_t max_count;                 // max entries of one head
+    int32_t max_abs;                   // max |offset| over all heads
+    int32_t start[kMaxHeads + 1];
+    int32_t off[kMaxEntries];
+};
+
+struct SupportImpl {
+    TableArg tab;
+    std::vector<int64_t> pairs;        // |Omega_h| per head
+};
+
+// ---- launch accounting (fibatt_launch_count) -------------------------------
+void count_launches(int n);
+
+// ---- error reporting (thread-local message) --------------------------------
+fibatt_status set_error(fibatt_status st, const std::string &msg);
+fibatt_status cuda_error(cudaError_t e, const char *what);
+
+// ---- launchers (return the CUDA launch status) -----------------------------
+struct FwdArgs {
+    const TableArg *tab;
+    int B;
+    fibatt_dtype dtype;
+    const void *Q, *K, *V;
+    void *O;
+    float *LSE;
+    float scale;
+    cudaStream_t stream;
+};
+
+struct BwdArgs {
+    const TableArg *tab;
+    int B;
+    fibatt_dtype dtype;
+    const void *Q, *K, *V, *O, *dO;
+    const float *LSE;
+    void *dQ, *dK, *dV;
+    float *Dws;                        // [B*H*N] fp32 scratch (generic path)
+    float scale;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_fwd_generic(const FwdArgs &a);
+cudaError_t launch_bwd_generic(const BwdArgs &a);
+
+}  // namespace fibatt

@@ -1,0 +1,73 @@
+"""Shared helpers for the GPU parity tests: seeded inputs, oracle heads,
+comparison against the oracle with the stated tolerances.
+
+Tolerances (fp32 accumulation throughout):
+  fp32 I/O: max |gpu - oracle| <= 1e-5 on O, LSE, dQ, dK, dV.
+  bf16 I/O: max |gpu - oracle| <= 2e-2 and mean |gpu - oracle| <= 2e-3 on
+            O, dQ, dK, dV (bf16 outputs); LSE is fp32 and held to 1e-4.
+"""
+import numpy as np
+import torch
+
+import oracle
+from sparse_head_self_gb300 import api
+from sparse_head_self_gb300.inputs import make_inputs
+
+TOL = {"f32": dict(max_abs=1e-5, mean_abs=1e-5), "bf16": dict(max_abs=2e-2, mean_abs=2e-3)}
+LSE_TOL = {"f32": 1e-5, "bf16": 1e-4}
+
+
+def oracle_heads(wl, modified=False):
+    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
+    heads = []
+    for i in range(1, wl.H + 1):
+        a, b = oracle.wythoff_row(i)
+        if modified:
+            a, b = 2 * a - b, b - a
+        heads.append(oracle.Head.fibottention(a, b, w[i - 1], wl.diag))
+    return heads
+
+
+def support_for(wl, modified=False):
+    return api.Support.wythoff(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag, modified=modified)
+
+
+def to_dev(*ts):
+    return [None if t is None else t.cuda() for t in ts]
+
+
+def assert_close(name, got, ref, dtype, lse=False):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), f"{name}: -inf pattern differs"
+    diff = np.abs(np.where(both_inf, 0.0, got - ref))
+    assert np.all(np.isfinite(diff)), f"{name}: non-finite values"
+    if lse:
+        tol = LSE_TOL[dtype]
+        assert diff.max() <= tol, f"{name}: max-abs {diff.max():.3e} > {tol:g}"
+        return
+    t = TOL[dtype]
+    assert diff.max() <= t["max_abs"], f"{name}: max-abs {diff.max():.3e} > {t['max_abs']:g}"
+    if dtype == "bf16":
+        assert diff.mean() <= t["mean_abs"], f"{name}: mean-abs {diff.mean():.3e} > {t['mean_abs']:g}"
+
+
+def pick_rows(N, count, seed):
+    """Edge rows plus a seeded random sample, sorted and unique."""
+    rng = np.random.default_rng(seed)
+    edge = [0, 1, 2, N // 2, N - 3, N - 2, N - 1]
+    rnd = rng.integers(0, N, size=max(0, count - len(edge))).tolist()
+    return sorted({r for r in edge + rnd if 0 <= r < N})
+
+
+def run_fwd(wl, sup, q, k, v):
+    qd, kd, vd = to_dev(q, k, v)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    torch.cuda.synchronize()
+    return O, L
+
+
+__all__ = ["TOL", "oracle_heads", "support_for", "to_dev", "assert_close", "pick_rows", "run_fwd",
+           "make_inputs"]

@@ -1,0 +1,208 @@
+"""GPU parity: libfibatt (through the C ABI) against the fp64 oracle.
+
+Small cases are compared element by element on every output; the full-size
+workloads, in the same launch configuration as bench.py, are compared on
+every output where the oracle is fast enough and on seeded row samples
+(edges included) otherwise.  Tolerances are in tests/gpu_helpers.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (assert_close, make_inputs, oracle_heads, pick_rows, support_for,
+                         to_dev)
+from sparse_head_self_gb300 import api
+from sparse_head_self_gb300.inputs import WORKLOADS, Workload
+
+pytestmark = pytest.mark.gpu
+
+oracle.set_threads(oracle.max_threads())
+
+
+def _fwd_full(wl, seed=0):
+    q, k, v, _ = make_inputs(wl, seed, with_grad=False)
+    sup = support_for(wl)
+    O, L = api.fwd(sup, *to_dev(q, k, v), wl.scale)
+    O_ref, L_ref = oracle.fwd(q, k, v, oracle_heads(wl), wl.scale)
+    assert_close(f"{wl.name} O", O.float().cpu(), O_ref, wl.dtype)
+    assert_close(f"{wl.name} LSE", L.cpu(), L_ref, wl.dtype, lse=True)
+
+
+def _bwd_full(wl, seed=0):
+    q, k, v, do = make_inputs(wl, seed)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    rQ, rK, rV = oracle.bwd(q, k, v, do, oracle_heads(wl), wl.scale)
+    assert_close(f"{wl.name} dQ", dQ.float().cpu(), rQ, wl.dtype)
+    assert_close(f"{wl.name} dK", dK.float().cpu(), rK, wl.dtype)
+    assert_close(f"{wl.name} dV", dV.float().cpu(), rV, wl.dtype)
+
+
+# ------------------------------------------------------------ small, full
+
+def test_tiny_fwd_fp32_full():
+    _fwd_full(WORKLOADS["tiny"])
+
+
+def test_tiny_bwd_fp32_full():
+    _bwd_full(WORKLOADS["tiny"])
+
+
+@pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_vitb_shape_small_batch_full(name, dtype):
+    wl = Workload(**{**WORKLOADS[name].__dict__, "B": 2, "dtype": dtype})
+    _fwd_full(wl, seed=5)
+    _bwd_full(wl, seed=5)
+
+
+def test_video_shape_one_batch_fwd_full():
+    wl = WORKLOADS["video"].with_batch(1)
+    _fwd_full(wl, seed=7)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 63, 64, 65, 127, 129, 300])
+@pytest.mark.parametrize("diag", [False, True])
+def test_edge_sizes(N, diag):
+    # rows 1..4 of the Wythoff array with windows up to N: includes heads whose
+    # whole support is empty (N <= a_h without the diagonal)
+    H = 4
+    wl = Workload("edge", 2, H, N, 64, "f32", 1, N, diag, True)
+    _fwd_full(wl, seed=N)
+    _bwd_full(wl, seed=N)
+
+
+def test_empty_support_rows_are_zero():
+    # N = 3, row 2 of the Wythoff array (4, 7), no diagonal: no pair at all
+    N = 3
+    sup = api.Support.build(N, [4], [7], [3], False)
+    q, k, v, do = (torch.randn(1, 1, N, 64, device="cuda") for _ in range(4))
+    O, L = api.fwd(sup, q, k, v, 0.125)
+    assert torch.all(O == 0) and torch.all(torch.isneginf(L))
+    dQ, dK, dV = api.bwd(sup, q, k, v, O, L, do, 0.125)
+    assert torch.all(dQ == 0) and torch.all(dK == 0) and torch.all(dV == 0)
+
+
+def test_diagonal_only_support_returns_V():
+    N = 77
+    sup = api.Support.from_distances(N, [[], []], True)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q, k, v = (torch.randn(3, 2, N, 64, device="cuda", generator=g) for _ in range(3))
+    O, L = api.fwd(sup, q, k, v, 0.125)
+    assert torch.equal(O, v)      # a single-term softmax has weight exactly 1
+    ref = 0.125 * (q.double() * k.double()).sum(-1)
+    assert (L.double() - ref).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_dense_support_equals_softmax_attention(dtype):
+    # every distance 0..N-1: plain softmax attention (checked against the oracle,
+    # itself pinned to library softmax attention)
+    N, H = 150, 2
+    wl = Workload("dense", 2, H, N, 64, dtype, 1, N, True, True)
+    q, k, v, do = make_inputs(wl, 11)
+    sup = api.Support.from_distances(N, [list(range(N))] * H, True)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    heads = [oracle.Head(range(N), N, True)] * H
+    O_ref, L_ref = oracle.fwd(q, k, v, heads, wl.scale)
+    assert_close("dense O", O.float().cpu(), O_ref, dtype)
+    assert_close("dense LSE", L.cpu(), L_ref, dtype, lse=True)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    rQ, rK, rV = oracle.bwd(q, k, v, do, heads, wl.scale)
+    for n, g, r in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV)):
+        assert_close(f"dense {n}", g.float().cpu(), r, dtype)
+
+
+def test_modified_wythoff_variant():
+    wl = WORKLOADS["tiny"]
+    q, k, v, do = make_inputs(wl, 13)
+    sup = support_for(wl, modified=True)
+    heads = oracle_heads(wl, modified=True)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    O_ref, L_ref = oracle.fwd(q, k, v, heads, wl.scale)
+    assert_close("mod O", O.cpu(), O_ref, "f32")
+    assert_close("mod LSE", L.cpu(), L_ref, "f32", lse=True)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    rQ, rK, rV = oracle.bwd(q, k, v, do, heads, wl.scale)
+    for n, g, r in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV)):
+        assert_close(f"mod {n}", g.cpu(), r, "f32")
+
+
+def test_autograd_function_matches_direct_calls():
+    wl = WORKLOADS["tiny"]
+    q, k, v, do = make_inputs(wl, 17)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    leaves = [t.clone().requires_grad_(True) for t in (qd, kd, vd)]
+    out = api.fibottention(*leaves, sup, wl.scale)
+    out.backward(dod)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    assert torch.equal(out, O)
+    for g, r in zip((leaves[0].grad, leaves[1].grad, leaves[2].grad), (dQ, dK, dV)):
+        assert torch.equal(g, r)
+
+
+def test_side_stream_and_repeatability():
+    wl = WORKLOADS["vitb"].with_batch(3)
+    q, k, v, _ = make_inputs(wl, 19, with_grad=False)
+    sup = support_for(wl)
+    qd, kd, vd = to_dev(q, k, v)
+    O1, L1 = api.fwd(sup, qd, kd, vd, wl.scale)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        O2, L2 = api.fwd(sup, qd, kd, vd, wl.scale, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+# ----------------------------------------------- full sizes, bench launches
+
+@pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
+def test_vitb_full_size_fwd_all_outputs(name):
+    _fwd_full(WORKLOADS[name])
+
+
+def _sampled(wl, nbh, nrows, seed, backward):
+    q, k, v, do = make_inputs(wl, 0, with_grad=backward)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    if backward:
+        dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    torch.cuda.synchronize()
+    heads = oracle_heads(wl)
+    rng = np.random.default_rng(seed)
+    picks = {(0, 0), (wl.B - 1, wl.H - 1)}
+    while len(picks) < nbh:
+        picks.add((int(rng.integers(wl.B)), int(rng.integers(wl.H))))
+    for (b, h) in sorted(picks):
+        rows = pick_rows(wl.N, nrows, seed + 31 * b + h)
+        Or, Lr = oracle.fwd_head(q[b, h], k[b, h], v[b, h], heads[h], wl.scale, rows=rows)
+        assert_close(f"{wl.name} O[{b},{h}]", O[b, h, rows].float().cpu(), Or, wl.dtype)
+        assert_close(f"{wl.name} LSE[{b},{h}]", L[b, h, rows].cpu(), Lr, wl.dtype, lse=True)
+        if backward:
+            rQ, rK, rV = oracle.bwd_head(q[b, h], k[b, h], v[b, h], do[b, h], heads[h], wl.scale,
+                                         qrows=rows, krows=rows)
+            assert_close(f"{wl.name} dQ[{b},{h}]", dQ[b, h, rows].float().cpu(), rQ, wl.dtype)
+            assert_close(f"{wl.name} dK[{b},{h}]", dK[b, h, rows].float().cpu(), rK, wl.dtype)
+            assert_close(f"{wl.name} dV[{b},{h}]", dV[b, h, rows].float().cpu(), rV, wl.dtype)
+
+
+def test_video_full_size_fwd_sampled():
+    _sampled(WORKLOADS["video"], nbh=12, nrows=48, seed=101, backward=True)
+
+
+def test_train_full_size_fwd_bwd_sampled():
+    _sampled(WORKLOADS["train"], nbh=24, nrows=40, seed=202, backward=True)
+
+
+def test_long_full_size_fwd_bwd_sampled():
+    _sampled(WORKLOADS["long"], nbh=6, nrows=12, seed=303, backward=True)
