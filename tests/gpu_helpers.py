@@ -42,7 +42,7 @@ def assert_close(name, got, ref, dtype, lse=False):
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     both_inf = np.isneginf(got) & np.isneginf(ref)
     assert np.array_equal(np.isneginf(got), np.isneginf(ref)), f"{name}: -inf pattern differs"
-    diff = np.abs(np.where(both_inf, 0.0, got - ref))
+    diff = np.abs(np.where(both_inf, 0.0, got) - np.where(both_inf, 0.0, ref))
     assert np.all(np.isfinite(diff)), f"{name}: non-finite values"
     if lse:
         tol = LSE_TOL[dtype]
