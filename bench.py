@@ -331,6 +331,10 @@ def gb300_arm(args):
     end.record()
     torch.cuda.synchronize(dev)
     launches = step.lib.fibatt_launch_count() - launches0
+    dev_err = ctypes.c_uint(0)
+    _native.check(step.lib.fibatt_device_error(1, ctypes.byref(dev_err)))
+    if dev_err.value:
+        raise SystemExit(f"device error word set during the timed region: {dev_err.value:#x}")
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)

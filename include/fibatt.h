@@ -162,6 +162,13 @@ const char *fibatt_last_error(void);
 /* Library version string. */
 const char *fibatt_version(void);
 
+/* Device-side error word of the current device: bit 0 (1) is set when a
+ * kernel gave up waiting for its shared-memory staging copies (a bounded wait
+ * of about 2 s; the kernel then returns without writing its outputs).  This
+ * call synchronises with the device.  With clear != 0 the word is reset.
+ * CUDA on a failed copy. */
+fibatt_status fibatt_device_error(int clear, unsigned *code);
+
 /* Number of CUDA kernels this library has launched in this process so far
  * (all devices, all threads); for accounting in benchmarks and tests. */
 uint64_t fibatt_launch_count(void);

@@ -47,6 +47,7 @@ _SIGS = {
     "fibatt_last_error": (ctypes.c_char_p, []),
     "fibatt_version": (ctypes.c_char_p, []),
     "fibatt_launch_count": (ctypes.c_uint64, []),
+    "fibatt_device_error": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint)]),
 }
 
 

@@ -54,6 +54,17 @@ int64_t int_sqrt(int64_t n) {
 // for n >= 1, so its floor can replace it.
 int64_t floor_phi(int64_t n) { return n <= 0 ? 0 : (n + int_sqrt(5 * n * n)) / 2; }
 
+// Kernel family override for tests and tuning: FIBATT_PATH=generic forces the
+// generic kernels, FIBATT_PATH=resident forbids falling back to them.
+enum class PathSel { Auto, Generic, Resident };
+PathSel path_sel() {
+    const char *e = std::getenv("FIBATT_PATH");
+    if (!e) return PathSel::Auto;
+    if (std::strcmp(e, "generic") == 0) return PathSel::Generic;
+    if (std::strcmp(e, "resident") == 0) return PathSel::Resident;
+    return PathSel::Auto;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Build one support from per-head distance sets (already cut to <= N-1).
@@ -252,7 +263,16 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     if (!LSE || !aligned(LSE, 4)) return set_error(FIBATT_ERR_INVALID_ARG, "LSE is NULL or misaligned");
     if (fault("launch")) return set_error(FIBATT_ERR_CUDA, "injected launch failure (FIBATT_FAULT=launch)");
     FwdArgs a{&s->impl.tab, B, dtype, Q, K, V, O, LSE, scale, stream};
-    cudaError_t e = launch_fwd_generic(a);
+    const PathSel sel = path_sel();
+    ResidentPlan pl;
+    cudaError_t e;
+    if (sel != PathSel::Generic && plan_fwd_resident(s->impl.tab, B, dtype, &pl)) {
+        e = launch_fwd_resident(a, pl);
+    } else {
+        if (sel == PathSel::Resident)
+            return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: windows do not fit in shared memory");
+        e = launch_fwd_generic(a);
+    }
     if (e != cudaSuccess) return cuda_error(e, "fibatt_fwd launch");
     return FIBATT_OK;
 }
@@ -293,5 +313,13 @@ const char *fibatt_last_error(void) { return g_last_error.c_str(); }
 const char *fibatt_version(void) { return "libfibatt 0.1 (sm_103a)"; }
 
 uint64_t fibatt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+fibatt_status fibatt_device_error(int clear, unsigned *code) {
+    if (!code) return set_error(FIBATT_ERR_INVALID_ARG, "code is NULL");
+    *code = 0;
+    cudaError_t e = read_device_error(code, clear != 0);
+    if (e != cudaSuccess) return cuda_error(e, "fibatt_device_error");
+    return FIBATT_OK;
+}
 
 }  // extern "C"

@@ -8,7 +8,7 @@
 
 #include <cuda_runtime_api.h>
 
-#include "../../include/fibatt.h"
+#include "fibatt.h"
 
 namespace fibatt {
 
@@ -66,7 +66,26 @@ struct BwdArgs {
     cudaStream_t stream;
 };
 
+// Shared-memory-resident kernels: one CTA per (b, h, query chunk); the
+// chunk's K/V row window is staged in shared memory (resident.cu).
+struct ResidentPlan {
+    int lanes;           // lanes per query row (2 or 4)
+    int qsplit;          // query chunks per (b, h)
+    int chunk;           // queries per chunk
+    int kv_cap;          // rows reserved per staged window
+    int stages;          // shared-memory ring depth
+    int groups;          // consumer warp groups
+    int gwarps;          // warps per consumer group
+    size_t stage_bytes;  // bytes per ring stage
+    size_t smem;         // dynamic shared memory bytes
+    int threads;         // threads per CTA (producer warp + consumers)
+    int grid;            // CTAs (persistent, one per SM at most)
+};
+bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl);
+
 cudaError_t launch_fwd_generic(const FwdArgs &a);
 cudaError_t launch_bwd_generic(const BwdArgs &a);
+cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl);
+cudaError_t read_device_error(unsigned *code, bool clear);
 
 }  // namespace fibatt

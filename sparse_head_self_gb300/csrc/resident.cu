@@ -1,0 +1,412 @@
+// Shared-memory-resident Fibottention kernels: persistent, warp-specialised,
+// TMA-fed.
+//
+// Work unit: (batch b, head h, query chunk [q0, q1)).  Because every offset
+// of a head is a fixed diagonal, the keys a chunk attends form the contiguous
+// row window [q0 + min_off, q1 + max_off) clipped to [0, N) (Fibottention
+// Sec. 3: |j - k| in Fib(a,b), |j - k| <= w), so one unit is three contiguous
+// row ranges: the chunk's Q rows and the K and V windows.
+//
+// One CTA per SM.  Warp 0 is the producer: one lane issues the three bulk
+// copies (TMA, cp.async.bulk) of each unit into a ring of shared-memory
+// stages, each stage guarded by a "full" mbarrier (byte count) and an "empty"
+// mbarrier (released by the consumer warps).  The other warps form consumer
+// groups; group g computes units g, g + groups, ... of this CTA, so loads of
+// later units overlap the arithmetic of earlier ones and HBM stays busy.
+// Every mbarrier wait is bounded in time (tma_common.cuh).
+//
+// Arithmetic (two lanes per query row, 32 dims each):
+//   s   = scale * <q_j, k_{j+d}>  -- bf16 x bf16 products with the
+//         mixed-precision fma.rn.f32.bf16 (exact products, fp32 sums),
+//         reduced over the lane pair with one xor-shuffle;
+//   online softmax in log2 units whose running maximum is only raised when
+//         a score exceeds it by more than 8 (then acc and l are rescaled),
+//         so the rescale is rare and p = 2^(s - m) <= 2^8 never overflows;
+//   acc += p * v_{j+d} with packed f32x2 fmas;
+//   O = acc / l (RNE to the I/O dtype), LSE = ln 2 * (m + log2 l).
+// Offsets that reach a key for every row of a warp's 16 rows run without
+// range predicates; only the edge offsets of a round are predicated.
+#include <algorithm>
+#include <cstdlib>
+#include <type_traits>
+
+#include "fibatt_internal.h"
+#include "tma_common.cuh"
+
+namespace fibatt {
+namespace {
+
+constexpr int kMaxStages = 4;
+
+struct PipeParams {
+    const void *Q, *K, *V;
+    void *O;
+    float *LSE;
+    float scale_log2;
+    int qsplit;        // query chunks per (b, h)
+    int chunk;         // queries per chunk (multiple of 16)
+    int kv_cap;        // rows reserved for each of the K and V windows
+    int n_units;       // B * H * qsplit
+    int stages;        // ring depth
+    int groups;        // consumer groups
+    int gwarps;        // warps per consumer group
+    uint32_t stage_bytes;
+};
+
+struct Unit {
+    int bh, h, q0, q1, t0, t1, lo, nrows;
+};
+
+__device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const PipeParams &p, int u) {
+    Unit g;
+    g.bh = u / p.qsplit;
+    g.h = g.bh % tab.H;
+    g.q0 = (u % p.qsplit) * p.chunk;
+    g.q1 = min(tab.N, g.q0 + p.chunk);
+    g.t0 = tab.start[g.h];
+    g.t1 = tab.start[g.h + 1];
+    g.lo = 0;
+    g.nrows = 0;
+    if (g.t1 > g.t0 && g.q1 > g.q0) {
+        g.lo = max(0, g.q0 + tab.off[g.t0]);
+        g.nrows = max(0, min(tab.N, g.q1 + tab.off[g.t1 - 1]) - g.lo);
+    }
+    return g;
+}
+
+template <int G>
+struct SoftmaxState {
+    float2 acc[32 / G];
+    float m, l;
+};
+
+template <int G>
+__device__ __forceinline__ void softmax_raise(SoftmaxState<G> &st, float s) {
+    if (s > st.m + 8.f) {
+        const float a = fast_exp2(st.m - s);
+        st.l *= a;
+#pragma unroll
+        for (int i = 0; i < 32 / G; ++i) st.acc[i] = mul2(st.acc[i], make_float2(a, a));
+        st.m = s;
+    }
+}
+
+// Per-lane geometry of a row slice: byte offsets of the lane's chunks.
+template <typename T, int G>
+struct LaneGeom {
+    using S = Slice<T, G>;
+    int c[S::kChunks];
+    __device__ __forceinline__ LaneGeom() {
+        const int lane = threadIdx.x & 31;
+        const int sub = lane % G, pos = (lane / G) % (8 / G);
+#pragma unroll
+        for (int i = 0; i < S::kChunks; ++i) c[i] = 16 * S::chunk(sub, pos, i);
+    }
+};
+
+// One pass over offsets [tb, te) (read from the shared-memory copy `off`)
+// for query row j.  PRED: some rows of the warp may fall outside [0, N) for
+// these offsets (or be padding rows).  Without PRED two offsets are handled
+// per step so that their shared-memory loads overlap.
+template <typename T, int G, bool PRED>
+__device__ __forceinline__ void fwd_offsets(const int *off, int N, int tb, int te, int j, bool valid, int lo,
+                                            const uint8_t *sK, int vdelta, const Slice<T, G> &q,
+                                            const LaneGeom<T, G> &lg, float sl2, SoftmaxState<G> &st) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    const uint8_t *base = sK + (ptrdiff_t)(j - lo) * RB;
+    int t = tb;
+    if (!PRED) {
+        for (; t + 1 < te; t += 2) {
+            const uint8_t *a0 = base + off[t] * RB, *a1 = base + off[t + 1] * RB;
+            S k0, k1;
+            k0.load(a0, lg.c);
+            k1.load(a1, lg.c);
+            float s0 = group_sum<G>(q.dot(k0)) * sl2;
+            float s1 = group_sum<G>(q.dot(k1)) * sl2;
+            softmax_raise(st, fmaxf(s0, s1));
+            const float p0 = fast_exp2(s0 - st.m), p1 = fast_exp2(s1 - st.m);
+            st.l += p0 + p1;
+            k0.load(a0 + vdelta, lg.c);
+            k1.load(a1 + vdelta, lg.c);
+            k0.axpy(p0, st.acc);
+            k1.axpy(p1, st.acc);
+        }
+    }
+    for (; t < te; ++t) {
+        const int k = j + off[t];
+        bool in = true;
+        const uint8_t *a = base + off[t] * RB;
+        if (PRED) {
+            in = valid && k >= 0 && k < N;
+            if (!in) a = sK;
+        }
+        S kv;
+        kv.load(a, lg.c);
+        const float s = group_sum<G>(q.dot(kv)) * sl2;
+        if (in) {
+            softmax_raise(st, s);
+            const float pr = fast_exp2(s - st.m);
+            st.l += pr;
+            kv.load(a + vdelta, lg.c);
+            kv.axpy(pr, st.acc);
+        }
+    }
+}
+
+// Offset index ranges of one round of rows [jfirst, jlast] of a head whose
+// ascending offsets are off[t0..t1): [tb, te) reach a key for some row,
+// [tf0, tf1) reach a key for every row.  Warp-collective (ballots).
+__device__ __forceinline__ void round_ranges(const int *off, int N, int t0, int t1, int jfirst, int jlast,
+                                             int &tb, int &te, int &tf0, int &tf1) {
+    const int lane = threadIdx.x & 31;
+    int below_last = 0, below_first = 0, above_first = 0, above_last = 0;
+    for (int base = t0; base < t1; base += 32) {
+        const int t = base + lane;
+        const bool e = t < t1;
+        const int o = e ? off[t] : 0;
+        below_last += __popc(__ballot_sync(kFullMask, e && jlast + o < 0));
+        below_first += __popc(__ballot_sync(kFullMask, e && jfirst + o < 0));
+        above_first += __popc(__ballot_sync(kFullMask, e && jfirst + o >= N));
+        above_last += __popc(__ballot_sync(kFullMask, e && jlast + o >= N));
+    }
+    tb = t0 + below_last;
+    te = t1 - above_first;
+    tf0 = max(tb, t0 + below_first);
+    tf1 = max(tf0, min(te, t1 - above_last));
+}
+
+template <typename T, int G>
+__device__ __forceinline__ void fwd_unit_rounds(const TableArg &tab, const int *off, const PipeParams &p,
+                                                const Unit &g, const uint8_t *sQ, const uint8_t *sK,
+                                                int vdelta, int wg, const LaneGeom<T, G> &lg) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;   // rows per warp round
+    const int N = tab.N;
+    const int lane = threadIdx.x & 31;
+    const size_t row0 = (size_t)g.bh * N;
+    T *gO = static_cast<T *>(p.O) + row0 * kHeadDim;
+    const int nq = g.q1 - g.q0, nrounds = (nq + R - 1) / R;
+    for (int r = wg; r < nrounds; r += p.gwarps) {
+        const int jl = r * R + lane / G;
+        const bool valid = jl < nq;
+        const int j = g.q0 + (valid ? jl : nq - 1);
+        const bool full = r * R + R <= nq;
+        const int jfirst = g.q0 + r * R;
+        const int jlast = g.q0 + min(nq, r * R + R) - 1;
+        int tb = g.t0, te = g.t0, tf0 = g.t0, tf1 = g.t0;
+        if (g.nrows) round_ranges(off, N, g.t0, g.t1, jfirst, jlast, tb, te, tf0, tf1);
+        if (!full) tf0 = tf1 = te;
+
+        S q;
+        q.load(sQ + (size_t)(j - g.q0) * RB, lg.c);
+        SoftmaxState<G> st;
+#pragma unroll
+        for (int i = 0; i < 32 / G; ++i) st.acc[i] = make_float2(0.f, 0.f);
+        st.m = -INFINITY;
+        st.l = 0.f;
+        fwd_offsets<T, G, true>(off, N, tb, tf0, j, valid, g.lo, sK, vdelta, q, lg, p.scale_log2, st);
+        fwd_offsets<T, G, false>(off, N, tf0, tf1, j, valid, g.lo, sK, vdelta, q, lg, p.scale_log2, st);
+        fwd_offsets<T, G, true>(off, N, tf1, te, j, valid, g.lo, sK, vdelta, q, lg, p.scale_log2, st);
+        if (valid) {
+            const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32 / G; ++i) st.acc[i] = mul2(st.acc[i], make_float2(inv, inv));
+            S::store(gO + (size_t)j * kHeadDim, lg.c, st.acc);
+            if (lane % G == 0) p.LSE[row0 + j] = st.l > 0.f ? (st.m + fast_log2(st.l)) * kLn2 : -INFINITY;
+        }
+    }
+}
+
+template <int G>
+constexpr int max_threads() { return G == 2 ? 512 : 1024; }
+
+template <typename T, int G>
+__global__ void __launch_bounds__(max_threads<G>(), 1)
+fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+    __shared__ int s_off[kMaxEntries];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], p.gwarps);
+        }
+    }
+    __syncthreads();
+
+    const size_t q_off = 0, k_off = (size_t)p.chunk * RB, v_off = k_off + (size_t)p.kv_cap * RB;
+    if (warp == 0) {
+        // producer: one lane streams every unit of this CTA into the ring
+        if (lane != 0) return;
+        int i = 0;
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+            const int s = i % p.stages;
+            if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
+            const Unit g = unit_geometry(tab, p, u);
+            uint8_t *st = smem + (size_t)s * p.stage_bytes;
+            const size_t row0 = (size_t)g.bh * tab.N;
+            const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
+            mbar_expect_tx(&full_bar[s], qb + 2 * kvb);
+            bulk_g2s(st + q_off, static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, qb, &full_bar[s]);
+            if (kvb) {
+                bulk_g2s(st + k_off, static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
+                bulk_g2s(st + v_off, static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
+            }
+        }
+        return;
+    }
+    // Consumers.  Use k of stage s is the CTA's unit i = s + k * stages, taken
+    // by group i % groups.  An mbarrier parity wait cannot tell a phase that
+    // completed from one two phases ahead, so before waiting for use k to be
+    // full the group waits for use k - 1 to be released.  That release wait is
+    // itself unambiguous when use k - 2 belonged to this group -- true when
+    // groups <= 2, or when stages is a multiple of groups (each stage then
+    // always serves the same group) -- the plan allows nothing else.
+    const int cw = warp - 1;
+    const int grp = cw / p.gwarps, wg = cw % p.gwarps;
+    if (grp >= p.groups) return;
+    const LaneGeom<T, G> lg;
+    int i = grp;
+    for (int u = blockIdx.x + grp * gridDim.x; u < p.n_units; u += p.groups * gridDim.x, i += p.groups) {
+        const int s = i % p.stages, k = i / p.stages;
+        if (k >= 1 && !mbar_wait(&empty_bar[s], (k - 1) & 1)) return;
+        if (!mbar_wait(&full_bar[s], k & 1)) return;
+        const Unit g = unit_geometry(tab, p, u);
+        const uint8_t *st = smem + (size_t)s * p.stage_bytes;
+        fwd_unit_rounds<T, G>(tab, s_off, p, g, st + q_off, st + k_off, (int)(v_off - k_off), wg, lg);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+}
+
+size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
+
+int g_sm_count[64] = {0};
+size_t g_fwd_smem_set[4][64] = {{0}};
+
+int sm_count(int dev) {
+    if (dev < 0 || dev >= 64) return 148;
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 148;
+    }
+    return g_sm_count[dev];
+}
+
+// Largest K/V window over every head and chunk.
+int window_cap(const TableArg &tab, int qsplit, int chunk) {
+    int cap = 1;
+    for (int h = 0; h < tab.H; ++h) {
+        const int t0 = tab.start[h], t1 = tab.start[h + 1];
+        if (t1 == t0) continue;
+        for (int c = 0; c < qsplit; ++c) {
+            const int q0 = c * chunk, q1 = std::min(tab.N, q0 + chunk);
+            if (q1 <= q0) continue;
+            cap = std::max(cap, std::min(tab.N, q1 + tab.off[t1 - 1]) - std::max(0, q0 + tab.off[t0]));
+        }
+    }
+    return cap;
+}
+
+}  // namespace
+
+// Plan of the pipelined resident forward; false when not even one stage fits
+// in shared memory (the generic kernel is used then).
+bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl) {
+    const int N = tab.N;
+    const size_t RB = row_bytes(dt);
+    const size_t budget = 210 * 1024;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int sms = sm_count(dev);
+    int G = 4;
+    if (const char *e = getenv("FIBATT_LANES")) G = atoi(e) == 2 ? 2 : 4;
+    const int R = 32 / G;                                  // rows per warp round
+    const int maxw = (G == 2 ? 512 : 1024) / 32;
+    // Query chunks of a multiple of R rows.  Aim for >= 8 units per SM and a
+    // ring of at least three stages.
+    int qsplit = 1;
+    const char *env = getenv("FIBATT_QSPLIT");
+    if (env) {
+        qsplit = std::max(1, atoi(env));
+    } else {
+        const long units = (long)B * tab.H;
+        while (qsplit < 64 && units * qsplit < 8L * sms && (N + qsplit) / (qsplit + 1) >= 32) ++qsplit;
+    }
+    int chunk = 0, kv_cap = 0;
+    size_t stage = 0;
+    for (;; ++qsplit) {
+        chunk = ((N + qsplit - 1) / qsplit + R - 1) / R * R;
+        const int qs = (N + chunk - 1) / chunk;
+        kv_cap = window_cap(tab, qs, chunk);
+        stage = ((size_t)chunk * RB + 2 * (size_t)kv_cap * RB + 127) / 128 * 128;
+        if (env || 3 * stage <= budget || chunk <= R) {
+            qsplit = qs;
+            break;
+        }
+    }
+    int stages = (int)std::min<size_t>(kMaxStages, budget / stage);
+    if (stages < 1) return false;
+    if (const char *e = getenv("FIBATT_STAGES")) stages = std::max(1, std::min(stages, atoi(e)));
+    // consumer groups: at most two (the kernel's release-then-full wait needs
+    // groups <= 2, or stages a multiple of groups)
+    int groups = stages >= 2 ? 2 : 1;
+    if (const char *e = getenv("FIBATT_GROUPS")) groups = std::max(1, std::min(2, atoi(e)));
+    const int rounds = chunk / R;
+    const int gwarps = std::max(1, std::min(rounds, (maxw - 1) / groups));
+    pl->lanes = G;
+    pl->qsplit = qsplit;
+    pl->chunk = chunk;
+    pl->kv_cap = kv_cap;
+    pl->stages = stages;
+    pl->groups = groups;
+    pl->gwarps = gwarps;
+    pl->stage_bytes = stage;
+    pl->smem = stage * stages;
+    pl->threads = 32 * (1 + groups * gwarps);
+    const long units = (long)B * tab.H * qsplit;
+    pl->grid = (int)std::min<long>(units, sms);
+    return true;
+}
+
+template <typename T, int G>
+static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int ti = (std::is_same<T, float>::value ? 0 : 2) + (G == 2 ? 0 : 1);
+    if (dev >= 0 && dev < 64 && g_fwd_smem_set[ti][dev] < pl.smem) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_pipe_kernel<T, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e != cudaSuccess) return e;
+        g_fwd_smem_set[ti][dev] = pl.smem;
+    }
+    PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
+                 a.B * a.tab->H * pl.qsplit, pl.stages, pl.groups, pl.gwarps, (uint32_t)pl.stage_bytes};
+    fwd_pipe_kernel<T, G><<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
+    if (a.dtype == FIBATT_F32)
+        return pl.lanes == 2 ? fwd_resident<float, 2>(a, pl) : fwd_resident<float, 4>(a, pl);
+    return pl.lanes == 2 ? fwd_resident<__nv_bfloat16, 2>(a, pl) : fwd_resident<__nv_bfloat16, 4>(a, pl);
+}
+
+// Read (and optionally clear) the device error word of the current device.
+cudaError_t read_device_error(unsigned *code, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned));
+    if (e != cudaSuccess || !clear || *code == 0) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace fibatt

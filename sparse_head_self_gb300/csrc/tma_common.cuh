@@ -1,0 +1,239 @@
+// Bulk-copy (TMA) and mbarrier helpers, inline PTX for sm_100+ / sm_103a, and
+// the row-slice arithmetic shared by the shared-memory-resident kernels.
+//
+// Every wait on an mbarrier is bounded by wall-clock time (%globaltimer):
+// after kWaitLimitNs the waiting thread records kErrWaitTimeout in the
+// device error word and the kernel returns, so a bad byte count can never hang
+// the GPU.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace fibatt {
+
+// Device error word (bit flags), read and cleared by fibatt_device_error().
+// Only resident.cu includes this header, so the word has one definition.
+static __device__ unsigned int g_device_error = 0;
+constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// One-dimensional bulk copy global -> this CTA's shared memory, completion
+// counted in bytes on `bar`.  dst/src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Plain arrive (count 1) on `bar`.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Wait for phase `parity` of `bar` to complete; false on timeout (error
+// recorded).  Each try_wait carries a suspend-time hint, so a waiting warp is
+// parked by the hardware until the phase completes (or about 0.5 ms pass)
+// instead of spinning and taking issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t b, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(b), "r"(parity), "r"(500000u)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t b = smem_u32(bar);
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(b, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_device_error, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+
+// ---- mixed-precision and packed fp32 arithmetic ----------------------------
+
+// c + lo(a)*lo(b) + hi(a)*hi(b) for packed bf16 pairs a, b.  Each product of
+// two bf16 values is exact in fp32, so this equals converting both operands
+// to fp32 and using fmaf, rounding for rounding.
+__device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
+    unsigned short al, ah, bl, bh;
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(al), "=h"(ah) : "r"(a));
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(bl), "=h"(bh) : "r"(b));
+    float d;
+    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(al), "h"(bl), "f"(c));
+    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(ah), "h"(bh), "f"(d));
+    return d;
+}
+
+// (c.x + a.x*b.x, c.y + a.y*b.y), each an IEEE fma (packed f32x2, sm_100+).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+// 2^x on the SFU (ex2.approx.ftz, relative error about 2^-22; results below
+// 2^-126 flush to zero, which only drops weights under 1e-38).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---- a slice of one 64-dim row ---------------------------------------------
+//
+// G lanes own one row, 64/G dims each (G = 2 or 4).  The lane at slot `sub`
+// (0..G-1) of the row at position `pos` (0..8/G-1: the row's slot inside an
+// eight-lane shared-memory phase) walks its 16-byte chunks in an order chosen
+// so that the eight lanes of each phase touch eight different bank groups:
+// rows are 128 B (bf16) or 256 B (fp32) and start on bank 0, so a chunk's
+// bank group is its index modulo 8.  `acc` holds the lane's dims as float2
+// pairs in the same chunk order.
+template <typename T, int G>
+struct Slice;
+
+template <int G>
+struct SliceBf16 {
+    static constexpr int kChunks = 8 / G;    // 16-byte chunks per lane
+    static constexpr int kRowBytes = 128;
+    static constexpr int kPairs = 32 / G;    // float2 accumulators per lane
+    __device__ static __forceinline__ int chunk(int sub, int pos, int i) {
+        return kChunks * sub + ((i + pos) % kChunks);
+    }
+    uint4 w[kChunks];                        // packed bf16 pairs
+
+    __device__ __forceinline__ void load(const uint8_t *row, const int (&c)[kChunks]) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) w[i] = *reinterpret_cast<const uint4 *>(row + c[i]);
+    }
+    // partial <this, o> over the lane's dims (four interleaved sums for ILP)
+    __device__ __forceinline__ float dot(const SliceBf16 &o) const {
+        float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            a = dot2_bf16(w[i].x, o.w[i].x, a);
+            b = dot2_bf16(w[i].y, o.w[i].y, b);
+            c = dot2_bf16(w[i].z, o.w[i].z, c);
+            d = dot2_bf16(w[i].w, o.w[i].w, d);
+        }
+        return (a + b) + (c + d);
+    }
+    // acc[4i + e] += p * (element pair e of chunk i)
+    __device__ __forceinline__ void axpy(float p, float2 (&acc)[kPairs]) const {
+        const float2 pp = make_float2(p, p);
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            acc[4 * i + 0] = fma2(pp, make_float2(bf16_lo(w[i].x), bf16_hi(w[i].x)), acc[4 * i + 0]);
+            acc[4 * i + 1] = fma2(pp, make_float2(bf16_lo(w[i].y), bf16_hi(w[i].y)), acc[4 * i + 1]);
+            acc[4 * i + 2] = fma2(pp, make_float2(bf16_lo(w[i].z), bf16_hi(w[i].z)), acc[4 * i + 2]);
+            acc[4 * i + 3] = fma2(pp, make_float2(bf16_lo(w[i].w), bf16_hi(w[i].w)), acc[4 * i + 3]);
+        }
+    }
+    // store acc (in this lane's chunk order) to a global row, RNE to bf16
+    __device__ __forceinline__ static void store(void *row, const int (&c)[kChunks], const float2 (&acc)[kPairs]) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            uint4 t;
+            t.x = pack_bf16x2(acc[4 * i + 0].x, acc[4 * i + 0].y);
+            t.y = pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y);
+            t.z = pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y);
+            t.w = pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y);
+            *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(row) + c[i]) = t;
+        }
+    }
+};
+
+template <int G>
+struct SliceF32 {
+    static constexpr int kChunks = 16 / G;
+    static constexpr int kRowBytes = 256;
+    static constexpr int kPairs = 32 / G;
+    // rows of 256 B: chunk c maps to bank group c mod 8
+    __device__ static __forceinline__ int chunk(int sub, int pos, int i) {
+        if (G == 2) return 8 * sub + ((i + 2 * pos + sub) & 7);
+        return 4 * sub + ((i + 2 * (sub >> 1) + pos) & 3);
+    }
+    float4 w[kChunks];
+
+    __device__ __forceinline__ void load(const uint8_t *row, const int (&c)[kChunks]) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) w[i] = *reinterpret_cast<const float4 *>(row + c[i]);
+    }
+    __device__ __forceinline__ float dot(const SliceF32 &o) const {
+        float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            a = fmaf(w[i].x, o.w[i].x, a);
+            b = fmaf(w[i].y, o.w[i].y, b);
+            c = fmaf(w[i].z, o.w[i].z, c);
+            d = fmaf(w[i].w, o.w[i].w, d);
+        }
+        return (a + b) + (c + d);
+    }
+    __device__ __forceinline__ void axpy(float p, float2 (&acc)[kPairs]) const {
+        const float2 pp = make_float2(p, p);
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            acc[2 * i + 0] = fma2(pp, make_float2(w[i].x, w[i].y), acc[2 * i + 0]);
+            acc[2 * i + 1] = fma2(pp, make_float2(w[i].z, w[i].w), acc[2 * i + 1]);
+        }
+    }
+    __device__ __forceinline__ static void store(void *row, const int (&c)[kChunks], const float2 (&acc)[kPairs]) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i)
+            *reinterpret_cast<float4 *>(static_cast<uint8_t *>(row) + c[i]) =
+                make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
+    }
+};
+
+template <int G>
+struct Slice<__nv_bfloat16, G> : SliceBf16<G> {};
+template <int G>
+struct Slice<float, G> : SliceF32<G> {};
+
+// Sum over the G lanes of a row (xor-shuffles).
+template <int G>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int m = 1; m < G; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+}  // namespace fibatt

@@ -31,3 +31,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error(request):
+    """After every GPU test: the library's device error word must be clear
+    (a bounded wait inside a kernel that gave up would have set it)."""
+    yield
+    if not HAS_GPU or "gpu" not in request.keywords:
+        return
+    import ctypes
+    import torch
+    from sparse_head_self_gb300 import _native
+    torch.cuda.synchronize()
+    code = ctypes.c_uint(0)
+    _native.check(_native.lib().fibatt_device_error(1, ctypes.byref(code)))
+    assert code.value == 0, f"device error word set: {code.value:#x}"

@@ -20,6 +20,17 @@ pytestmark = pytest.mark.gpu
 oracle.set_threads(oracle.max_threads())
 
 
+@pytest.fixture
+def kernel_path(request, monkeypatch):
+    """Select the kernel family through FIBATT_PATH for one test."""
+    path = getattr(request, "param", "auto")
+    if path == "auto":
+        monkeypatch.delenv("FIBATT_PATH", raising=False)
+    else:
+        monkeypatch.setenv("FIBATT_PATH", path)
+    return path
+
+
 def _fwd_full(wl, seed=0):
     q, k, v, _ = make_inputs(wl, seed, with_grad=False)
     sup = support_for(wl)
@@ -43,7 +54,8 @@ def _bwd_full(wl, seed=0):
 
 # ------------------------------------------------------------ small, full
 
-def test_tiny_fwd_fp32_full():
+@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+def test_tiny_fwd_fp32_full(kernel_path):
     _fwd_full(WORKLOADS["tiny"])
 
 
@@ -51,9 +63,10 @@ def test_tiny_bwd_fp32_full():
     _bwd_full(WORKLOADS["tiny"])
 
 
+@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
 @pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_vitb_shape_small_batch_full(name, dtype):
+def test_vitb_shape_small_batch_full(name, dtype, kernel_path):
     wl = Workload(**{**WORKLOADS[name].__dict__, "B": 2, "dtype": dtype})
     _fwd_full(wl, seed=5)
     _bwd_full(wl, seed=5)
@@ -64,9 +77,10 @@ def test_video_shape_one_batch_fwd_full():
     _fwd_full(wl, seed=7)
 
 
+@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 63, 64, 65, 127, 129, 300])
 @pytest.mark.parametrize("diag", [False, True])
-def test_edge_sizes(N, diag):
+def test_edge_sizes(N, diag, kernel_path):
     # rows 1..4 of the Wythoff array with windows up to N: includes heads whose
     # whole support is empty (N <= a_h without the diagonal)
     H = 4
@@ -75,7 +89,18 @@ def test_edge_sizes(N, diag):
     _bwd_full(wl, seed=N)
 
 
-def test_empty_support_rows_are_zero():
+@pytest.mark.parametrize("qsplit", ["1", "2", "3", "7", "40"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_resident_query_chunks(qsplit, dtype, monkeypatch):
+    # every split of the 197 queries into chunks, ragged last chunk included
+    monkeypatch.setenv("FIBATT_PATH", "resident")
+    monkeypatch.setenv("FIBATT_QSPLIT", qsplit)
+    wl = Workload(**{**WORKLOADS["vitb"].__dict__, "B": 2, "dtype": dtype})
+    _fwd_full(wl, seed=23)
+
+
+@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+def test_empty_support_rows_are_zero(kernel_path):
     # N = 3, row 2 of the Wythoff array (4, 7), no diagonal: no pair at all
     N = 3
     sup = api.Support.build(N, [4], [7], [3], False)
@@ -86,7 +111,8 @@ def test_empty_support_rows_are_zero():
     assert torch.all(dQ == 0) and torch.all(dK == 0) and torch.all(dV == 0)
 
 
-def test_diagonal_only_support_returns_V():
+@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+def test_diagonal_only_support_returns_V(kernel_path):
     N = 77
     sup = api.Support.from_distances(N, [[], []], True)
     g = torch.Generator(device="cuda").manual_seed(3)
@@ -97,8 +123,9 @@ def test_diagonal_only_support_returns_V():
     assert (L.double() - ref).abs().max().item() <= 1e-5
 
 
+@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_dense_support_equals_softmax_attention(dtype):
+def test_dense_support_equals_softmax_attention(dtype, kernel_path):
     # every distance 0..N-1: plain softmax attention (checked against the oracle,
     # itself pinned to library softmax attention)
     N, H = 150, 2
@@ -117,7 +144,8 @@ def test_dense_support_equals_softmax_attention(dtype):
         assert_close(f"dense {n}", g.float().cpu(), r, dtype)
 
 
-def test_modified_wythoff_variant():
+@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
+def test_modified_wythoff_variant(kernel_path):
     wl = WORKLOADS["tiny"]
     q, k, v, do = make_inputs(wl, 13)
     sup = support_for(wl, modified=True)
@@ -168,6 +196,14 @@ def test_side_stream_and_repeatability():
 @pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
 def test_vitb_full_size_fwd_all_outputs(name):
     _fwd_full(WORKLOADS[name])
+
+
+def test_no_device_error_recorded():
+    import ctypes
+    from sparse_head_self_gb300 import _native
+    code = ctypes.c_uint(123)
+    _native.check(_native.lib().fibatt_device_error(1, ctypes.byref(code)))
+    assert code.value == 0
 
 
 def _sampled(wl, nbh, nrows, seed, backward):
