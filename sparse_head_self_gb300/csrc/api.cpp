@@ -283,6 +283,13 @@ size_t fibatt_bwd_workspace_bytes(fibatt_support_t s, int B) {
     return (rows * sizeof(float) + 255) / 256 * 256;
 }
 
+// Workspace the chosen backward path actually touches (0 for the resident
+// kernel, which keeps its scratch in shared memory).
+static size_t bwd_workspace_needed(fibatt_support_t s, int B, fibatt_dtype dt, bool *resident, ResidentPlan *pl) {
+    *resident = path_sel() != PathSel::Generic && plan_bwd_resident(s->impl.tab, B, dt, pl);
+    return *resident ? 0 : fibatt_bwd_workspace_bytes(s, B);
+}
+
 fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
                          const void *V, const void *O, const float *LSE, const void *dO, float scale, void *dQ,
                          void *dK, void *dV, void *workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -293,7 +300,11 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
         (st = check_tensor(dK, "dK")) || (st = check_tensor(dV, "dV")))
         return st;
     if (!LSE || !aligned(LSE, 4)) return set_error(FIBATT_ERR_INVALID_ARG, "LSE is NULL or misaligned");
-    const size_t need = fibatt_bwd_workspace_bytes(s, B);
+    bool resident = false;
+    ResidentPlan pl;
+    const size_t need = bwd_workspace_needed(s, B, dtype, &resident, &pl);
+    if (!resident && path_sel() == PathSel::Resident)
+        return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: the backward does not fit in shared memory");
     if (need > 0) {
         if ((st = check_tensor(workspace, "workspace"))) return st;
         if (ws_bytes < need)
@@ -303,7 +314,7 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     if (fault("launch")) return set_error(FIBATT_ERR_CUDA, "injected launch failure (FIBATT_FAULT=launch)");
     BwdArgs a{&s->impl.tab, B, dtype, Q, K, V, O, dO, LSE, dQ, dK, dV, static_cast<float *>(workspace),
               scale, stream};
-    cudaError_t e = launch_bwd_generic(a);
+    cudaError_t e = resident ? launch_bwd_resident(a, pl) : launch_bwd_generic(a);
     if (e != cudaSuccess) return cuda_error(e, "fibatt_bwd launch");
     return FIBATT_OK;
 }

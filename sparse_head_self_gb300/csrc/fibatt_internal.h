@@ -82,10 +82,12 @@ struct ResidentPlan {
     int grid;            // CTAs (persistent, one per SM at most)
 };
 bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl);
+bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl);
 
 cudaError_t launch_fwd_generic(const FwdArgs &a);
 cudaError_t launch_bwd_generic(const BwdArgs &a);
 cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl);
+cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
 
 }  // namespace fibatt

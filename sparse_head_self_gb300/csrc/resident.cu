@@ -286,10 +286,223 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     }
 }
 
+// ---------------------------------------------------------------- backward
+//
+// Work unit: one (batch b, head h), whole sequence resident.  A stage holds
+// the head's Q, K, V and dO rows (four bulk copies); the producer also
+// prefetches the next unit's O rows and LSE into L2.  All consumer warps share
+// a unit in two phases separated by a named barrier:
+//   A (query-centric, row j): s = <q_j, k>, dP = <dO_j, v> for k = j + off[t];
+//     P = exp(s - LSE_j), dS = P (dP - D_j) with D_j = <dO_j, O_j>;
+//     dQ_j = scale * sum dS k; P and dS go to a shared scratch [t][j].
+//   B (key-centric, row k): the tables are symmetric (built from distances),
+//     so the queries attending key k are j = k + off[t'] over the same table,
+//     and the pair's forward offset index is the mirror t0 + t1 - 1 - t';
+//     dK_k = scale * sum dS q_j, dV_k = sum P dO_j -- each key row owned by
+//     one lane group, no atomics.
+
+struct BwdParams {
+    const void *Q, *K, *V, *O, *dO;
+    const float *LSE;
+    void *dQ, *dK, *dV;
+    float scale, scale_log2;
+    int n_units;       // B * H
+    int stages;        // ring depth (1 or 2)
+    int cwarps;        // consumer warps
+    uint32_t stage_bytes;
+    uint32_t scratch_off;   // byte offset of the P/dS scratch in dynamic smem
+    int max_count;          // max table entries of one head (scratch rows)
+};
+
+// Phase A for one round of query rows.
+template <typename T, int G, bool PRED>
+__device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int tb, int te, int j, bool valid,
+                                              const uint8_t *sK, int vdelta, const Slice<T, G> &q,
+                                              const Slice<T, G> &g, float Dj, float lse2, float sl2,
+                                              const LaneGeom<T, G> &lg, float *scrP, float *scrS,
+                                              float2 (&dq)[32 / G]) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    const bool writer = (threadIdx.x & (G - 1)) == 0;
+    for (int t = tb; t < te; ++t) {
+        const int k = j + off[t];
+        bool in = true;
+        const uint8_t *a = sK + (ptrdiff_t)k * RB;
+        if (PRED) {
+            in = valid && k >= 0 && k < N;
+            if (!in) a = sK;
+        }
+        S kk, vv;
+        kk.load(a, lg.c);
+        vv.load(a + vdelta, lg.c);
+        const float s = group_sum<G>(q.dot(kk));
+        const float dp = group_sum<G>(g.dot(vv));
+        if (in) {
+            const float P = fast_exp2(fmaf(s, sl2, -lse2));
+            const float dS = P * (dp - Dj);
+            if (writer) {
+                scrP[(t - t0) * N + j] = P;
+                scrS[(t - t0) * N + j] = dS;
+            }
+            kk.axpy(dS, dq);
+        }
+    }
+}
+
+// Phase B for one round of key rows.
+template <typename T, int G, bool PRED>
+__device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int t1, int tb, int te, int k,
+                                              bool valid, const uint8_t *sQ, int gdelta,
+                                              const LaneGeom<T, G> &lg, const float *scrP, const float *scrS,
+                                              float2 (&dk)[32 / G], float2 (&dv)[32 / G]) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    for (int t = tb; t < te; ++t) {
+        const int j = k + off[t];
+        bool in = true;
+        if (PRED) in = valid && j >= 0 && j < N;
+        if (in) {
+            const int m = t0 + t1 - 1 - t;            // forward offset index of the pair (j, k)
+            const float P = scrP[(m - t0) * N + j];
+            const float dS = scrS[(m - t0) * N + j];
+            const uint8_t *a = sQ + (ptrdiff_t)j * RB;
+            S qq, gg;
+            qq.load(a, lg.c);
+            gg.load(a + gdelta, lg.c);
+            qq.axpy(dS, dk);
+            gg.axpy(P, dv);
+        }
+    }
+}
+
+// MAXT: threads per CTA the register budget is sized for (65536 / MAXT each).
+template <typename T, int G, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1)
+bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full_bar[2], empty_bar[2];
+    __shared__ int s_off[kMaxEntries];
+
+    const int N = tab.N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+    }
+    __syncthreads();
+    const size_t tens = (size_t)N * RB;   // one tensor's rows in a stage: Q | K | V | dO
+    if (warp == 0) {
+        if (lane != 0) return;
+        int i = 0;
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+            const int s = i % p.stages;
+            if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
+            uint8_t *st = smem + (size_t)s * p.stage_bytes;
+            const size_t row0 = (size_t)u * N;
+            const uint32_t b = (uint32_t)tens;
+            mbar_expect_tx(&full_bar[s], 4 * b);
+            bulk_g2s(st, static_cast<const T *>(p.Q) + row0 * kHeadDim, b, &full_bar[s]);
+            bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
+            bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
+            bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
+            const int un = u + gridDim.x;
+            if (un < p.n_units) {
+                bulk_prefetch_l2(static_cast<const T *>(p.O) + (size_t)un * N * kHeadDim, b);
+                if ((N * 4) % 16 == 0 && ((size_t)un * N * 4) % 16 == 0)
+                    bulk_prefetch_l2(p.LSE + (size_t)un * N, (uint32_t)N * 4);
+            }
+        }
+        return;
+    }
+    const int cw = warp - 1;
+    if (cw >= p.cwarps) return;
+    const int cthreads = 32 * p.cwarps;
+    const LaneGeom<T, G> lg;
+    float *scrP = reinterpret_cast<float *>(smem + p.scratch_off);
+    float *scrS = scrP + (size_t)p.max_count * N;
+    const int nrounds = (N + R - 1) / R;
+    int i = 0;
+    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+        const int s = i % p.stages;
+        if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
+        const uint8_t *st = smem + (size_t)s * p.stage_bytes;
+        const uint8_t *sQ = st, *sK = st + tens;
+        const int h = u % tab.H;
+        const int t0 = tab.start[h], t1 = tab.start[h + 1];
+        const size_t row0 = (size_t)u * N;
+        // ---- phase A: query rows
+        for (int r = cw; r < nrounds; r += p.cwarps) {
+            const int jl = r * R + lane / G;
+            const bool valid = jl < N;
+            const int j = valid ? jl : N - 1;
+            const bool full = r * R + R <= N;
+            const int jfirst = r * R, jlast = min(N, r * R + R) - 1;
+            int tb = t0, te = t0, tf0 = t0, tf1 = t0;
+            if (t1 > t0) round_ranges(s_off, N, t0, t1, jfirst, jlast, tb, te, tf0, tf1);
+            if (!full) tf0 = tf1 = te;
+            S q, g, o;
+            q.load(sQ + (size_t)j * RB, lg.c);
+            g.load(sQ + 3 * tens + (size_t)j * RB, lg.c);
+            o.load_global(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim, lg.c);
+            const float Dj = group_sum<G>(g.dot(o));
+            const float lse2 = p.LSE[row0 + j] * kLog2e;
+            float2 dq[32 / G];
+#pragma unroll
+            for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
+            const int vd = (int)tens;
+            bwd_a_offsets<T, G, true>(s_off, N, t0, tb, tf0, j, valid, sK, vd, q, g, Dj, lse2, p.scale_log2, lg,
+                                      scrP, scrS, dq);
+            bwd_a_offsets<T, G, false>(s_off, N, t0, tf0, tf1, j, valid, sK, vd, q, g, Dj, lse2, p.scale_log2,
+                                       lg, scrP, scrS, dq);
+            bwd_a_offsets<T, G, true>(s_off, N, t0, tf1, te, j, valid, sK, vd, q, g, Dj, lse2, p.scale_log2, lg,
+                                      scrP, scrS, dq);
+            if (valid) {
+#pragma unroll
+                for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
+                S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
+            }
+        }
+        consumer_sync(cthreads);
+        // ---- phase B: key rows
+        for (int r = cw; r < nrounds; r += p.cwarps) {
+            const int kl = r * R + lane / G;
+            const bool valid = kl < N;
+            const int k = valid ? kl : N - 1;
+            const bool full = r * R + R <= N;
+            const int kfirst = r * R, klast = min(N, r * R + R) - 1;
+            int tb = t0, te = t0, tf0 = t0, tf1 = t0;
+            if (t1 > t0) round_ranges(s_off, N, t0, t1, kfirst, klast, tb, te, tf0, tf1);
+            if (!full) tf0 = tf1 = te;
+            float2 dk[32 / G], dv[32 / G];
+#pragma unroll
+            for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
+            const int gd = (int)(3 * tens);
+            bwd_b_offsets<T, G, true>(s_off, N, t0, t1, tb, tf0, k, valid, sQ, gd, lg, scrP, scrS, dk, dv);
+            bwd_b_offsets<T, G, false>(s_off, N, t0, t1, tf0, tf1, k, valid, sQ, gd, lg, scrP, scrS, dk, dv);
+            bwd_b_offsets<T, G, true>(s_off, N, t0, t1, tf1, te, k, valid, sQ, gd, lg, scrP, scrS, dk, dv);
+            if (valid) {
+#pragma unroll
+                for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
+                S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
+                S::store(static_cast<T *>(p.dV) + (row0 + k) * kHeadDim, lg.c, dv);
+            }
+        }
+        consumer_sync(cthreads);   // scratch and stage free for the next unit
+        if (cw == 0 && lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+}
+
 size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
 
 int g_sm_count[64] = {0};
 size_t g_fwd_smem_set[4][64] = {{0}};
+size_t g_bwd_smem_set[4][64] = {{0}};
 
 int sm_count(int dev) {
     if (dev < 0 || dev >= 64) return 148;
@@ -393,6 +606,64 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     fwd_pipe_kernel<T, G><<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// Plan of the resident backward: the whole head's Q, K, V, dO in one stage,
+// plus a P/dS scratch of max_count x N floats each.  False when one stage and
+// the scratch do not fit.
+bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl) {
+    const int N = tab.N;
+    const size_t RB = row_bytes(dt);
+    const size_t budget = 218 * 1024;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int sms = sm_count(dev);
+    const int G = 4, R = 32 / G;
+    int maxt = 512;
+    if (const char *e = getenv("FIBATT_BWD_THREADS")) maxt = atoi(e) == 1024 ? 1024 : 512;
+    const int maxw = maxt / 32;
+    const size_t stage = (4 * (size_t)N * RB + 127) / 128 * 128;
+    const size_t scratch = (2 * (size_t)std::max(1, tab.max_count) * N * 4 + 127) / 128 * 128;
+    int stages = stage * 2 + scratch <= budget ? 2 : (stage + scratch <= budget ? 1 : 0);
+    if (const char *e = getenv("FIBATT_STAGES")) stages = std::min(stages, std::max(1, atoi(e)));
+    if (stages < 1) return false;
+    const int rounds = (N + R - 1) / R;
+    pl->lanes = G;
+    pl->qsplit = 1;
+    pl->chunk = N;
+    pl->kv_cap = N;
+    pl->stages = stages;
+    pl->groups = 1;
+    pl->gwarps = std::max(1, std::min(rounds, maxw - 1));
+    pl->stage_bytes = stage;
+    pl->smem = stage * stages + scratch;
+    pl->threads = 32 * (1 + pl->gwarps);
+    pl->grid = (int)std::min<long>((long)B * tab.H, sms);
+    return true;
+}
+
+template <typename T>
+static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int ti = std::is_same<T, float>::value ? 0 : 1;
+    auto kern = pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>;
+    const int ki = ti * 2 + (pl.threads > 512 ? 1 : 0);
+    if (dev >= 0 && dev < 64 && g_bwd_smem_set[ki][dev] < pl.smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e != cudaSuccess) return e;
+        g_bwd_smem_set[ki][dev] = pl.smem;
+    }
+    BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
+                a.B * a.tab->H, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
+                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count)};
+    kern<<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
+    return a.dtype == FIBATT_F32 ? bwd_resident<float>(a, pl) : bwd_resident<__nv_bfloat16>(a, pl);
 }
 
 cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {

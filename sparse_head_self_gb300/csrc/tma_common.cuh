@@ -51,6 +51,16 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Hint that [src, src + bytes) will be read soon: bulk prefetch into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Barrier among the first `threads` threads past warp 0 (named barrier 1).
+__device__ __forceinline__ void consumer_sync(int threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
 // Plain arrive (count 1) on `bar`.
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -143,6 +153,11 @@ struct SliceBf16 {
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) w[i] = *reinterpret_cast<const uint4 *>(row + c[i]);
     }
+    __device__ __forceinline__ void load_global(const void *row, const int (&c)[kChunks]) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i)
+            w[i] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(row) + c[i]));
+    }
     // partial <this, o> over the lane's dims (four interleaved sums for ILP)
     __device__ __forceinline__ float dot(const SliceBf16 &o) const {
         float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
@@ -195,6 +210,11 @@ struct SliceF32 {
     __device__ __forceinline__ void load(const uint8_t *row, const int (&c)[kChunks]) {
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) w[i] = *reinterpret_cast<const float4 *>(row + c[i]);
+    }
+    __device__ __forceinline__ void load_global(const void *row, const int (&c)[kChunks]) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i)
+            w[i] = __ldg(reinterpret_cast<const float4 *>(static_cast<const uint8_t *>(row) + c[i]));
     }
     __device__ __forceinline__ float dot(const SliceF32 &o) const {
         float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
