@@ -144,8 +144,11 @@ def test_support_build_errors():
         api.window_schedule(3, 10, 5)
 
 
-def test_fwd_argument_errors_without_launch():
+def test_fwd_argument_errors_without_launch(monkeypatch):
     L = _native.lib()
+    # the generic backward takes a workspace, so its size check runs (and
+    # fails) before anything could be launched with the fake pointers below
+    monkeypatch.setenv("FIBATT_PATH", "generic")
     sup = api.Support.wythoff(3, 65, 5, 65, True)
     fake = 1 << 20  # never dereferenced: every case below fails its checks first
     lse = 1 << 21
