@@ -156,6 +156,25 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype,
                          void *dQ, void *dK, void *dV, void *workspace, size_t ws_bytes,
                          cudaStream_t stream);
 
+/* Scratch rows (fp32 each) built into the library for fibatt_bwd_noalloc. */
+#define FIBATT_NOALLOC_MAX_ROWS (1u << 20)
+
+/* Backward pass for callers that cannot allocate device memory (for example
+ * code that runs where the allocator is off limits, or a plugin that is
+ * handed fixed buffers).  Same arguments, results and errors as fibatt_bwd
+ * without the workspace: the scratch (one fp32 per query row) lives in a
+ * fixed array of FIBATT_NOALLOC_MAX_ROWS rows that every GPU loading the
+ * library holds until the process exits, so this call allocates nothing.
+ * INVALID_ARG when B*H*N exceeds FIBATT_NOALLOC_MAX_ROWS.  The first call on
+ * a device looks up the array's device address on that device (make it before
+ * any stream capture).  All calls on a device share the array: calls that
+ * overlap on the GPU race on it.  No counterpart in the paper: this is a
+ * library convenience, not part of the method. */
+fibatt_status fibatt_bwd_noalloc(fibatt_support_t s, int B, int D, fibatt_dtype dtype,
+                                 const void *Q, const void *K, const void *V, const void *O,
+                                 const float *LSE, const void *dO, float scale,
+                                 void *dQ, void *dK, void *dV, cudaStream_t stream);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char *fibatt_last_error(void);
 

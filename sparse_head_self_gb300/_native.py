@@ -44,6 +44,8 @@ _SIGS = {
     "fibatt_bwd": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
                                   _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                   _vp]),
+    "fibatt_bwd_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                          _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]),
     "fibatt_last_error": (ctypes.c_char_p, []),
     "fibatt_version": (ctypes.c_char_p, []),
     "fibatt_launch_count": (ctypes.c_uint64, []),

@@ -213,6 +213,26 @@ def bwd(support: Support, Q, K, V, O, LSE, dO, scale: float, dQ=None, dK=None, d
     return dQ, dK, dV
 
 
+def bwd_noalloc(support: Support, Q, K, V, O, LSE, dO, scale: float, dQ, dK, dV, stream=None):
+    """fibatt_bwd_noalloc: the backward pass without any workspace argument, for
+    callers that must not allocate device memory (its scratch is a fixed array
+    inside the library; at most B*H*N = FIBATT_NOALLOC_MAX_ROWS rows).  The
+    output tensors dQ, dK, dV are required and written in place."""
+    B, H, N, D = Q.shape
+    if (H, N) != (support.H, support.N):
+        raise ValueError(f"tensors have H={H}, N={N}; support has H={support.H}, N={support.N}")
+    if Q.dtype not in _DTYPES:
+        raise ValueError(f"dtype {Q.dtype} unsupported (float32 or bfloat16)")
+    dev = Q.device
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+        _check_io(n, t, Q.shape, Q.dtype, dev)
+    _check_io("LSE", LSE, (B, H, N), torch.float32, dev)
+    check(lib().fibatt_bwd_noalloc(support.handle, B, D, _DTYPES[Q.dtype], Q.data_ptr(), K.data_ptr(),
+                                   V.data_ptr(), O.data_ptr(), LSE.data_ptr(), dO.data_ptr(), float(scale),
+                                   dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), _stream_ptr(stream, dev)))
+    return dQ, dK, dV
+
+
 class FibottentionFunction(torch.autograd.Function):
     """Autograd wrapper: forward = fibatt_fwd, backward = fibatt_bwd."""
 
@@ -239,5 +259,5 @@ def fibottention(Q, K, V, support: Support, scale: float | None = None):
     return FibottentionFunction.apply(Q, K, V, support, float(scale))
 
 
-__all__ = ["FibattError", "Support", "fwd", "bwd", "fibottention", "FibottentionFunction",
+__all__ = ["FibattError", "Support", "fwd", "bwd", "bwd_noalloc", "fibottention", "FibottentionFunction",
            "wythoff_row", "wythoff_row_modified", "window_schedule", "HEAD_DIM"]

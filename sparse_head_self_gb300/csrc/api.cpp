@@ -140,6 +140,21 @@ fibatt_status set_error(fibatt_status st, const std::string &msg) {
     return st;
 }
 
+fibatt_status check_bwd_args(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
+                             const void *V, const void *O, const float *LSE, const void *dO, float scale,
+                             const void *dQ, const void *dK, const void *dV) {
+    fibatt_status st = check_common(s, B, D, dtype, scale);
+    if (st != FIBATT_OK) return st;
+    if ((st = check_tensor(Q, "Q")) || (st = check_tensor(K, "K")) || (st = check_tensor(V, "V")) ||
+        (st = check_tensor(O, "O")) || (st = check_tensor(dO, "dO")) || (st = check_tensor(dQ, "dQ")) ||
+        (st = check_tensor(dK, "dK")) || (st = check_tensor(dV, "dV")))
+        return st;
+    if (!LSE || !aligned(LSE, 4)) return set_error(FIBATT_ERR_INVALID_ARG, "LSE is NULL or misaligned");
+    return FIBATT_OK;
+}
+
+const TableArg &support_table(fibatt_support_t s) { return s->impl.tab; }
+
 fibatt_status cuda_error(cudaError_t e, const char *what) {
     cudaGetLastError();  // clear a sticky-free launch error so the next call starts clean
     return set_error(FIBATT_ERR_CUDA, fmt("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e)));

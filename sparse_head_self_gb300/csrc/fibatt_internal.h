@@ -42,6 +42,12 @@ void count_launches(int n);
 fibatt_status set_error(fibatt_status st, const std::string &msg);
 fibatt_status cuda_error(cudaError_t e, const char *what);
 
+// Argument checks of fibatt_bwd minus the workspace, and a support's tables.
+fibatt_status check_bwd_args(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
+                             const void *V, const void *O, const float *LSE, const void *dO, float scale,
+                             const void *dQ, const void *dK, const void *dV);
+const TableArg &support_table(fibatt_support_t s);
+
 // ---- launchers (return the CUDA launch status) -----------------------------
 struct FwdArgs {
     const TableArg *tab;
