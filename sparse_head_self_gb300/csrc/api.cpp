@@ -7,8 +7,11 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
 #include <set>
+#include <tuple>
 #include <string>
 #include <vector>
 
@@ -140,6 +143,64 @@ fibatt_status set_error(fibatt_status st, const std::string &msg) {
     return st;
 }
 
+namespace {
+struct PlanKey {
+    const void *support;
+    bool backward;
+    int B, dt, dev;
+    std::string env;
+    bool operator<(const PlanKey &o) const {
+        return std::tie(support, backward, B, dt, dev, env) < std::tie(o.support, o.backward, o.B, o.dt, o.dev, o.env);
+    }
+};
+struct PlanEntry {
+    bool ok;
+    ResidentPlan plan;
+};
+std::mutex g_plan_mu;
+std::map<PlanKey, PlanEntry> g_plans;
+
+std::string tuning_env() {
+    std::string r;
+    for (const char *n : {"FIBATT_QSPLIT", "FIBATT_LANES", "FIBATT_GROUPS", "FIBATT_STAGES", "FIBATT_BWD_THREADS"}) {
+        const char *e = std::getenv(n);
+        r += e ? e : "-";
+        r += ',';
+    }
+    return r;
+}
+}  // namespace
+
+bool cached_plan(const void *support, bool backward, const TableArg &tab, int B, fibatt_dtype dt,
+                 ResidentPlan *pl) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    PlanKey key{support, backward, B, (int)dt, dev, tuning_env()};
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            *pl = it->second.plan;
+            return it->second.ok;
+        }
+    }
+    PlanEntry e;
+    e.ok = backward ? plan_bwd_resident(tab, B, dt, &e.plan) : plan_fwd_resident(tab, B, dt, &e.plan);
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    if (g_plans.size() > 4096) g_plans.clear();
+    g_plans[key] = e;
+    *pl = e.plan;
+    return e.ok;
+}
+
+void forget_plans(const void *support) {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (auto it = g_plans.begin(); it != g_plans.end();) {
+        if (it->first.support == support) it = g_plans.erase(it);
+        else ++it;
+    }
+}
+
 fibatt_status check_bwd_args(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
                              const void *V, const void *O, const float *LSE, const void *dO, float scale,
                              const void *dQ, const void *dK, const void *dV) {
@@ -266,7 +327,10 @@ fibatt_status fibatt_support_get(fibatt_support_t s, int32_t *counts, int32_t *s
     return FIBATT_OK;
 }
 
-void fibatt_support_destroy(fibatt_support_t s) { delete s; }
+void fibatt_support_destroy(fibatt_support_t s) {
+    if (s) forget_plans(s);
+    delete s;
+}
 
 fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
                          const void *V, float scale, void *O, float *LSE, cudaStream_t stream) {
@@ -281,7 +345,7 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     const PathSel sel = path_sel();
     ResidentPlan pl;
     cudaError_t e;
-    if (sel != PathSel::Generic && plan_fwd_resident(s->impl.tab, B, dtype, &pl)) {
+    if (sel != PathSel::Generic && cached_plan(s, false, s->impl.tab, B, dtype, &pl)) {
         e = launch_fwd_resident(a, pl);
     } else {
         if (sel == PathSel::Resident)
@@ -301,7 +365,7 @@ size_t fibatt_bwd_workspace_bytes(fibatt_support_t s, int B) {
 // Workspace the chosen backward path actually touches (0 for the resident
 // kernel, which keeps its scratch in shared memory).
 static size_t bwd_workspace_needed(fibatt_support_t s, int B, fibatt_dtype dt, bool *resident, ResidentPlan *pl) {
-    *resident = path_sel() != PathSel::Generic && plan_bwd_resident(s->impl.tab, B, dt, pl);
+    *resident = path_sel() != PathSel::Generic && cached_plan(s, true, s->impl.tab, B, dt, pl);
     return *resident ? 0 : fibatt_bwd_workspace_bytes(s, B);
 }
 

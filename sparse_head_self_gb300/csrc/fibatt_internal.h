@@ -30,6 +30,8 @@ struct TableArg {
     int32_t off[kMaxEntries];
 };
 
+struct ResidentPlan;
+
 struct SupportImpl {
     TableArg tab;
     std::vector<int64_t> pairs;        // |Omega_h| per head
@@ -89,6 +91,13 @@ struct ResidentPlan {
 };
 bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl);
 bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan *pl);
+
+// Plans memoised per (support, B, dtype, device, tuning overrides): planning
+// is host work that would otherwise run on every call.
+struct PlanCache;
+bool cached_plan(const void *support, bool backward, const TableArg &tab, int B, fibatt_dtype dt,
+                 ResidentPlan *pl);
+void forget_plans(const void *support);
 
 cudaError_t launch_fwd_generic(const FwdArgs &a);
 cudaError_t launch_bwd_generic(const BwdArgs &a);

@@ -554,9 +554,17 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
         const long units = (long)B * tab.H;
         while (qsplit < 64 && units * qsplit < 8L * sms && (N + qsplit) / (qsplit + 1) >= 32) ++qsplit;
     }
+    // Smallest possible stage (one round of rows): if even that does not fit,
+    // the windows are too wide for this kernel.
+    {
+        const int qs_min = (N + R - 1) / R;
+        const size_t smallest = (size_t)R * RB + 2 * (size_t)window_cap(tab, qs_min, R) * RB;
+        if (smallest > budget) return false;
+    }
     int chunk = 0, kv_cap = 0;
     size_t stage = 0;
-    for (;; ++qsplit) {
+    // grow the split geometrically until three stages fit (or rows run out)
+    for (;; qsplit = std::max(qsplit + 1, qsplit * 5 / 4)) {
         chunk = ((N + qsplit - 1) / qsplit + R - 1) / R * R;
         const int qs = (N + chunk - 1) / chunk;
         kv_cap = window_cap(tab, qs, chunk);
