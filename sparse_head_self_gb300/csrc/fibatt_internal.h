@@ -78,12 +78,15 @@ struct BwdArgs {
 // chunk's K/V row window is staged in shared memory (resident.cu).
 struct ResidentPlan {
     int lanes;           // lanes per query row (2 or 4)
+    int unroll;          // offsets per step in the interior loop (1 or 2)
+    int maxt;            // threads the kernel's register budget is sized for
     int qsplit;          // query chunks per (b, h)
     int chunk;           // queries per chunk
     int kv_cap;          // rows reserved per staged window
     int stages;          // shared-memory ring depth
     int groups;          // consumer warp groups
     int gwarps;          // warps per consumer group
+    int prefetch;        // units beyond the ring warmed in L2 (forward)
     size_t stage_bytes;  // bytes per ring stage
     size_t smem;         // dynamic shared memory bytes
     int threads;         // threads per CTA (producer warp + consumers)

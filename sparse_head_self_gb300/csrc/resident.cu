@@ -51,6 +51,7 @@ struct PipeParams {
     int groups;        // consumer groups
     int gwarps;        // warps per consumer group
     uint32_t stage_bytes;
+    int prefetch;      // units beyond the ring warmed in L2
 };
 
 struct Unit {
@@ -104,129 +105,136 @@ struct LaneGeom {
     }
 };
 
-// One pass over offsets [tb, te) (read from the shared-memory copy `off`)
-// for query row j.  PRED: some rows of the warp may fall outside [0, N) for
-// these offsets (or be padding rows).  Without PRED two offsets are handled
-// per step so that their shared-memory loads overlap.
-template <typename T, int G, bool PRED>
+// Running-max start: finite, so a prefix of masked scores (-inf) gives
+// 2^(-inf - m) = 0 instead of a NaN, and any real score raises it.
+constexpr float kMaxInit = -1.0e30f;
+
+// One pass over offsets [tb, te) (read from the shared-memory copy `off`) for
+// query row j, branch-free: the key row is clamped into the staged window
+// [lo, lo + nrows) and a score whose key lies outside [0, N) (or whose row is
+// padding) becomes -inf, so its weight is exactly 0 and the raise never
+// triggers.  Two offsets per step so their shared-memory loads overlap.
+template <typename T, int G, int UNROLL>
 __device__ __forceinline__ void fwd_offsets(const int *off, int N, int tb, int te, int j, bool valid, int lo,
-                                            const uint8_t *sK, int vdelta, const Slice<T, G> &q,
+                                            int nrows, const uint8_t *sK, int vdelta, const Slice<T, G> &q,
                                             const LaneGeom<T, G> &lg, float sl2, SoftmaxState<G> &st) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
-    const uint8_t *base = sK + (ptrdiff_t)(j - lo) * RB;
+    const int kmin = max(lo, 0), kmax = min(lo + nrows, N) - 1;   // keys present in the window
     int t = tb;
-    if (!PRED) {
+    if (UNROLL == 2) {
         for (; t + 1 < te; t += 2) {
-            const uint8_t *a0 = base + off[t] * RB, *a1 = base + off[t + 1] * RB;
-            S k0, k1;
-            k0.load(a0, lg.c);
-            k1.load(a1, lg.c);
-            float s0 = group_sum<G>(q.dot(k0)) * sl2;
-            float s1 = group_sum<G>(q.dot(k1)) * sl2;
+            const int k0 = j + off[t], k1 = j + off[t + 1];
+            const bool in0 = valid && k0 >= 0 && k0 < N, in1 = valid && k1 >= 0 && k1 < N;
+            const uint8_t *a0 = sK + (ptrdiff_t)(min(max(k0, kmin), kmax) - lo) * RB;
+            const uint8_t *a1 = sK + (ptrdiff_t)(min(max(k1, kmin), kmax) - lo) * RB;
+            S k0r, k1r;
+            k0r.load(a0, lg.c);
+            k1r.load(a1, lg.c);
+            float s0 = group_sum<G>(q.dot(k0r)) * sl2;
+            float s1 = group_sum<G>(q.dot(k1r)) * sl2;
+            s0 = in0 ? s0 : -INFINITY;
+            s1 = in1 ? s1 : -INFINITY;
             softmax_raise(st, fmaxf(s0, s1));
             const float p0 = fast_exp2(s0 - st.m), p1 = fast_exp2(s1 - st.m);
             st.l += p0 + p1;
-            k0.load(a0 + vdelta, lg.c);
-            k1.load(a1 + vdelta, lg.c);
-            k0.axpy(p0, st.acc);
-            k1.axpy(p1, st.acc);
+            k0r.load(a0 + vdelta, lg.c);
+            k1r.load(a1 + vdelta, lg.c);
+            k0r.axpy(p0, st.acc);
+            k1r.axpy(p1, st.acc);
         }
     }
     for (; t < te; ++t) {
         const int k = j + off[t];
-        bool in = true;
-        const uint8_t *a = base + off[t] * RB;
-        if (PRED) {
-            in = valid && k >= 0 && k < N;
-            if (!in) a = sK;
-        }
+        const bool in = valid && k >= 0 && k < N;
+        const uint8_t *a = sK + (ptrdiff_t)(min(max(k, kmin), kmax) - lo) * RB;
         S kv;
         kv.load(a, lg.c);
-        const float s = group_sum<G>(q.dot(kv)) * sl2;
-        if (in) {
-            softmax_raise(st, s);
-            const float pr = fast_exp2(s - st.m);
-            st.l += pr;
-            kv.load(a + vdelta, lg.c);
-            kv.axpy(pr, st.acc);
-        }
+        float s = group_sum<G>(q.dot(kv)) * sl2;
+        s = in ? s : -INFINITY;
+        softmax_raise(st, s);
+        const float pr = fast_exp2(s - st.m);
+        st.l += pr;
+        kv.load(a + vdelta, lg.c);
+        kv.axpy(pr, st.acc);
     }
 }
 
-// Offset index ranges of one round of rows [jfirst, jlast] of a head whose
-// ascending offsets are off[t0..t1): [tb, te) reach a key for some row,
-// [tf0, tf1) reach a key for every row.  Warp-collective (ballots).
-__device__ __forceinline__ void round_ranges(const int *off, int N, int t0, int t1, int jfirst, int jlast,
-                                             int &tb, int &te, int &tf0, int &tf1) {
+// Offsets of a head (ascending off[t0..t1)) that reach a key in [0, N) for
+// at least one row of the round [jfirst, jlast]: [tb, te).  Warp-collective.
+__device__ __forceinline__ void round_range(const int *off, int N, int t0, int t1, int jfirst, int jlast, int &tb,
+                                            int &te) {
     const int lane = threadIdx.x & 31;
-    int below_last = 0, below_first = 0, above_first = 0, above_last = 0;
+    int below = 0, above = 0;
     for (int base = t0; base < t1; base += 32) {
         const int t = base + lane;
         const bool e = t < t1;
         const int o = e ? off[t] : 0;
-        below_last += __popc(__ballot_sync(kFullMask, e && jlast + o < 0));
-        below_first += __popc(__ballot_sync(kFullMask, e && jfirst + o < 0));
-        above_first += __popc(__ballot_sync(kFullMask, e && jfirst + o >= N));
-        above_last += __popc(__ballot_sync(kFullMask, e && jlast + o >= N));
+        below += __popc(__ballot_sync(kFullMask, e && jlast + o < 0));
+        above += __popc(__ballot_sync(kFullMask, e && jfirst + o >= N));
     }
-    tb = t0 + below_last;
-    te = t1 - above_first;
-    tf0 = max(tb, t0 + below_first);
-    tf1 = max(tf0, min(te, t1 - above_last));
+    tb = t0 + below;
+    te = max(tb, t1 - above);
 }
 
-template <typename T, int G>
-__device__ __forceinline__ void fwd_unit_rounds(const TableArg &tab, const int *off, const PipeParams &p,
-                                                const Unit &g, const uint8_t *sQ, const uint8_t *sK,
-                                                int vdelta, int wg, const LaneGeom<T, G> &lg) {
+// Round r of a unit: query rows [q0 + r R, q0 + r R + R) with R = 32 / G.
+template <typename T, int G, int UNROLL>
+__device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, const PipeParams &p, const Unit &g,
+                                          const uint8_t *sQ, const uint8_t *sK, int vdelta, int r,
+                                          const LaneGeom<T, G> &lg) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
-    constexpr int R = 32 / G;   // rows per warp round
+    constexpr int R = 32 / G;
     const int N = tab.N;
     const int lane = threadIdx.x & 31;
+    const int nq = g.q1 - g.q0;
+    if (r * R >= nq) return;
     const size_t row0 = (size_t)g.bh * N;
     T *gO = static_cast<T *>(p.O) + row0 * kHeadDim;
-    const int nq = g.q1 - g.q0, nrounds = (nq + R - 1) / R;
-    for (int r = wg; r < nrounds; r += p.gwarps) {
-        const int jl = r * R + lane / G;
-        const bool valid = jl < nq;
-        const int j = g.q0 + (valid ? jl : nq - 1);
-        const bool full = r * R + R <= nq;
-        const int jfirst = g.q0 + r * R;
-        const int jlast = g.q0 + min(nq, r * R + R) - 1;
-        int tb = g.t0, te = g.t0, tf0 = g.t0, tf1 = g.t0;
-        if (g.nrows) round_ranges(off, N, g.t0, g.t1, jfirst, jlast, tb, te, tf0, tf1);
-        if (!full) tf0 = tf1 = te;
+    const int jl = r * R + lane / G;
+    const bool valid = jl < nq;
+    const int j = g.q0 + (valid ? jl : nq - 1);
+    const int jfirst = g.q0 + r * R;
+    const int jlast = g.q0 + min(nq, r * R + R) - 1;
+    int tb = g.t0, te = g.t0;
+    if (g.nrows) round_range(off, N, g.t0, g.t1, jfirst, jlast, tb, te);
 
-        S q;
-        q.load(sQ + (size_t)(j - g.q0) * RB, lg.c);
-        SoftmaxState<G> st;
+    S q;
+    q.load(sQ + (size_t)(j - g.q0) * RB, lg.c);
+    SoftmaxState<G> st;
 #pragma unroll
-        for (int i = 0; i < 32 / G; ++i) st.acc[i] = make_float2(0.f, 0.f);
-        st.m = -INFINITY;
-        st.l = 0.f;
-        fwd_offsets<T, G, true>(off, N, tb, tf0, j, valid, g.lo, sK, vdelta, q, lg, p.scale_log2, st);
-        fwd_offsets<T, G, false>(off, N, tf0, tf1, j, valid, g.lo, sK, vdelta, q, lg, p.scale_log2, st);
-        fwd_offsets<T, G, true>(off, N, tf1, te, j, valid, g.lo, sK, vdelta, q, lg, p.scale_log2, st);
-        if (valid) {
-            const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+    for (int i = 0; i < 32 / G; ++i) st.acc[i] = make_float2(0.f, 0.f);
+    st.m = kMaxInit;
+    st.l = 0.f;
+    fwd_offsets<T, G, UNROLL>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
+    if (valid) {
+        const float inv = st.l > 0.f ? __frcp_rn(st.l) : 0.f;
 #pragma unroll
-            for (int i = 0; i < 32 / G; ++i) st.acc[i] = mul2(st.acc[i], make_float2(inv, inv));
-            S::store(gO + (size_t)j * kHeadDim, lg.c, st.acc);
-            if (lane % G == 0) p.LSE[row0 + j] = st.l > 0.f ? (st.m + fast_log2(st.l)) * kLn2 : -INFINITY;
-        }
+        for (int i = 0; i < 32 / G; ++i) st.acc[i] = mul2(st.acc[i], make_float2(inv, inv));
+        S::store(gO + (size_t)j * kHeadDim, lg.c, st.acc);
+        if (lane % G == 0) p.LSE[row0 + j] = st.l > 0.f ? (st.m + fast_log2(st.l)) * kLn2 : -INFINITY;
     }
 }
 
-template <int G>
-constexpr int max_threads() { return G == 2 ? 512 : 1024; }
+// L2 prefetch of unit u's three row ranges (a hint: nothing waits on it).
+template <typename T>
+__device__ __forceinline__ void prefetch_unit(const TableArg &tab, const PipeParams &p, int u) {
+    constexpr int RB = sizeof(T) * kHeadDim;
+    const Unit g = unit_geometry(tab, p, u);
+    const size_t row0 = (size_t)g.bh * tab.N;
+    bulk_prefetch_l2(static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, (uint32_t)(g.q1 - g.q0) * RB);
+    if (g.nrows) {
+        bulk_prefetch_l2(static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, (uint32_t)g.nrows * RB);
+        bulk_prefetch_l2(static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, (uint32_t)g.nrows * RB);
+    }
+}
 
-template <typename T, int G>
-__global__ void __launch_bounds__(max_threads<G>(), 1)
+template <typename T, int G, int UNROLL, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1)
 fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     __shared__ int s_off[kMaxEntries];
@@ -243,11 +251,17 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
 
     const size_t q_off = 0, k_off = (size_t)p.chunk * RB, v_off = k_off + (size_t)p.kv_cap * RB;
     if (warp == 0) {
-        // producer: one lane streams every unit of this CTA into the ring
+        // producer: one lane streams every unit of this CTA into the ring and
+        // keeps the next `prefetch` units warming in L2
         if (lane != 0) return;
         int i = 0;
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
             const int s = i % p.stages;
+            if (i == 0)
+                for (int d = p.stages; d < p.stages + p.prefetch; ++d) {
+                    const int un = u + d * gridDim.x;
+                    if (un < p.n_units) prefetch_unit<T>(tab, p, un);
+                }
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
             const Unit g = unit_geometry(tab, p, u);
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
@@ -258,6 +272,10 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
             if (kvb) {
                 bulk_g2s(st + k_off, static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
                 bulk_g2s(st + v_off, static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
+            }
+            if (i >= 1 && p.prefetch > 0) {
+                const int un = u + (p.stages + p.prefetch - 1) * gridDim.x;
+                if (un < p.n_units) prefetch_unit<T>(tab, p, un);
             }
         }
         return;
@@ -273,6 +291,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     const int grp = cw / p.gwarps, wg = cw % p.gwarps;
     if (grp >= p.groups) return;
     const LaneGeom<T, G> lg;
+    const int rpu = p.chunk / R;
     int i = grp;
     for (int u = blockIdx.x + grp * gridDim.x; u < p.n_units; u += p.groups * gridDim.x, i += p.groups) {
         const int s = i % p.stages, k = i / p.stages;
@@ -280,7 +299,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         if (!mbar_wait(&full_bar[s], k & 1)) return;
         const Unit g = unit_geometry(tab, p, u);
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
-        fwd_unit_rounds<T, G>(tab, s_off, p, g, st + q_off, st + k_off, (int)(v_off - k_off), wg, lg);
+        for (int r = wg; r < rpu; r += p.gwarps)
+            fwd_round<T, G, UNROLL>(tab, s_off, p, g, st + q_off, st + k_off, (int)(v_off - k_off), r, lg);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -314,8 +334,10 @@ struct BwdParams {
     int max_count;          // max table entries of one head (scratch rows)
 };
 
-// Phase A for one round of query rows.
-template <typename T, int G, bool PRED>
+// Phase A for one round of query rows, branch-free: the key row is clamped
+// into [0, N) and an out-of-range pair gets P = 0 (so dS = 0 too); only
+// in-range pairs are written to the scratch.
+template <typename T, int G>
 __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int tb, int te, int j, bool valid,
                                               const uint8_t *sK, int vdelta, const Slice<T, G> &q,
                                               const Slice<T, G> &g, float Dj, float lse2, float sl2,
@@ -326,31 +348,26 @@ __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int
     const bool writer = (threadIdx.x & (G - 1)) == 0;
     for (int t = tb; t < te; ++t) {
         const int k = j + off[t];
-        bool in = true;
-        const uint8_t *a = sK + (ptrdiff_t)k * RB;
-        if (PRED) {
-            in = valid && k >= 0 && k < N;
-            if (!in) a = sK;
-        }
+        const bool in = valid && k >= 0 && k < N;
+        const uint8_t *a = sK + (ptrdiff_t)min(max(k, 0), N - 1) * RB;
         S kk, vv;
         kk.load(a, lg.c);
         vv.load(a + vdelta, lg.c);
         const float s = group_sum<G>(q.dot(kk));
         const float dp = group_sum<G>(g.dot(vv));
-        if (in) {
-            const float P = fast_exp2(fmaf(s, sl2, -lse2));
-            const float dS = P * (dp - Dj);
-            if (writer) {
-                scrP[(t - t0) * N + j] = P;
-                scrS[(t - t0) * N + j] = dS;
-            }
-            kk.axpy(dS, dq);
+        const float P = in ? fast_exp2(fmaf(s, sl2, -lse2)) : 0.f;
+        const float dS = P * (dp - Dj);
+        if (writer && in) {
+            scrP[(t - t0) * N + j] = P;
+            scrS[(t - t0) * N + j] = dS;
         }
+        kk.axpy(dS, dq);
     }
 }
 
-// Phase B for one round of key rows.
-template <typename T, int G, bool PRED>
+// Phase B for one round of key rows, branch-free: the query row is clamped
+// into [0, N) and an out-of-range pair contributes P = dS = 0.
+template <typename T, int G>
 __device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int t1, int tb, int te, int k,
                                               bool valid, const uint8_t *sQ, int gdelta,
                                               const LaneGeom<T, G> &lg, const float *scrP, const float *scrS,
@@ -359,19 +376,17 @@ __device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int
     constexpr int RB = S::kRowBytes;
     for (int t = tb; t < te; ++t) {
         const int j = k + off[t];
-        bool in = true;
-        if (PRED) in = valid && j >= 0 && j < N;
-        if (in) {
-            const int m = t0 + t1 - 1 - t;            // forward offset index of the pair (j, k)
-            const float P = scrP[(m - t0) * N + j];
-            const float dS = scrS[(m - t0) * N + j];
-            const uint8_t *a = sQ + (ptrdiff_t)j * RB;
-            S qq, gg;
-            qq.load(a, lg.c);
-            gg.load(a + gdelta, lg.c);
-            qq.axpy(dS, dk);
-            gg.axpy(P, dv);
-        }
+        const bool in = valid && j >= 0 && j < N;
+        const int jc = min(max(j, 0), N - 1);
+        const int m = t0 + t1 - 1 - t;            // forward offset index of the pair (j, k)
+        const float P = in ? scrP[(m - t0) * N + jc] : 0.f;
+        const float dS = in ? scrS[(m - t0) * N + jc] : 0.f;
+        const uint8_t *a = sQ + (ptrdiff_t)jc * RB;
+        S qq, gg;
+        qq.load(a, lg.c);
+        gg.load(a + gdelta, lg.c);
+        qq.axpy(dS, dk);
+        gg.axpy(P, dv);
     }
 }
 
@@ -441,11 +456,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             const int jl = r * R + lane / G;
             const bool valid = jl < N;
             const int j = valid ? jl : N - 1;
-            const bool full = r * R + R <= N;
             const int jfirst = r * R, jlast = min(N, r * R + R) - 1;
-            int tb = t0, te = t0, tf0 = t0, tf1 = t0;
-            if (t1 > t0) round_ranges(s_off, N, t0, t1, jfirst, jlast, tb, te, tf0, tf1);
-            if (!full) tf0 = tf1 = te;
+            int tb = t0, te = t0;
+            if (t1 > t0) round_range(s_off, N, t0, t1, jfirst, jlast, tb, te);
             S q, g, o;
             q.load(sQ + (size_t)j * RB, lg.c);
             g.load(sQ + 3 * tens + (size_t)j * RB, lg.c);
@@ -455,13 +468,8 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             float2 dq[32 / G];
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
-            const int vd = (int)tens;
-            bwd_a_offsets<T, G, true>(s_off, N, t0, tb, tf0, j, valid, sK, vd, q, g, Dj, lse2, p.scale_log2, lg,
-                                      scrP, scrS, dq);
-            bwd_a_offsets<T, G, false>(s_off, N, t0, tf0, tf1, j, valid, sK, vd, q, g, Dj, lse2, p.scale_log2,
-                                       lg, scrP, scrS, dq);
-            bwd_a_offsets<T, G, true>(s_off, N, t0, tf1, te, j, valid, sK, vd, q, g, Dj, lse2, p.scale_log2, lg,
-                                      scrP, scrS, dq);
+            bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (int)tens, q, g, Dj, lse2, p.scale_log2, lg,
+                                scrP, scrS, dq);
             if (valid) {
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
@@ -474,18 +482,13 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             const int kl = r * R + lane / G;
             const bool valid = kl < N;
             const int k = valid ? kl : N - 1;
-            const bool full = r * R + R <= N;
             const int kfirst = r * R, klast = min(N, r * R + R) - 1;
-            int tb = t0, te = t0, tf0 = t0, tf1 = t0;
-            if (t1 > t0) round_ranges(s_off, N, t0, t1, kfirst, klast, tb, te, tf0, tf1);
-            if (!full) tf0 = tf1 = te;
+            int tb = t0, te = t0;
+            if (t1 > t0) round_range(s_off, N, t0, t1, kfirst, klast, tb, te);
             float2 dk[32 / G], dv[32 / G];
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
-            const int gd = (int)(3 * tens);
-            bwd_b_offsets<T, G, true>(s_off, N, t0, t1, tb, tf0, k, valid, sQ, gd, lg, scrP, scrS, dk, dv);
-            bwd_b_offsets<T, G, false>(s_off, N, t0, t1, tf0, tf1, k, valid, sQ, gd, lg, scrP, scrS, dk, dv);
-            bwd_b_offsets<T, G, true>(s_off, N, t0, t1, tf1, te, k, valid, sQ, gd, lg, scrP, scrS, dk, dv);
+            bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (int)(3 * tens), lg, scrP, scrS, dk, dv);
             if (valid) {
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
@@ -501,7 +504,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
 
 int g_sm_count[64] = {0};
-size_t g_fwd_smem_set[4][64] = {{0}};
+size_t g_fwd_smem_set[16][64] = {{0}};
 size_t g_bwd_smem_set[4][64] = {{0}};
 
 int sm_count(int dev) {
@@ -540,10 +543,15 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     int dev = 0;
     cudaGetDevice(&dev);
     const int sms = sm_count(dev);
-    int G = 4;
+    // two lanes per row measured fastest on the ViT-B shape (tuning overrides below)
+    int G = 2, unroll = 2, maxt = 1024;
     if (const char *e = getenv("FIBATT_LANES")) G = atoi(e) == 2 ? 2 : 4;
+    if (G == 2) maxt = 512;
+    if (const char *e = getenv("FIBATT_UNROLL")) unroll = atoi(e) == 1 ? 1 : 2;
+    if (const char *e = getenv("FIBATT_FWD_THREADS")) maxt = atoi(e) == 768 ? 768 : (atoi(e) == 512 ? 512 : 1024);
+    if (G == 4) maxt = 1024;
     const int R = 32 / G;                                  // rows per warp round
-    const int maxw = (G == 2 ? 512 : 1024) / 32;
+    const int maxw = maxt / 32;
     // Query chunks of a multiple of R rows.  Aim for >= 8 units per SM and a
     // ring of at least three stages.
     int qsplit = 1;
@@ -583,7 +591,12 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     if (const char *e = getenv("FIBATT_GROUPS")) groups = std::max(1, std::min(2, atoi(e)));
     const int rounds = chunk / R;
     const int gwarps = std::max(1, std::min(rounds, (maxw - 1) / groups));
+    int prefetch = 0;   // L2 warming of later units measured slower: off by default
+    if (const char *e = getenv("FIBATT_PREFETCH")) prefetch = std::max(0, std::min(8, atoi(e)));
+    pl->prefetch = prefetch;
     pl->lanes = G;
+    pl->unroll = unroll;
+    pl->maxt = maxt;
     pl->qsplit = qsplit;
     pl->chunk = chunk;
     pl->kv_cap = kv_cap;
@@ -598,22 +611,31 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     return true;
 }
 
-template <typename T, int G>
+template <typename T, int G, int UNROLL, int MAXT>
 static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     int dev = 0;
     cudaGetDevice(&dev);
-    const int ti = (std::is_same<T, float>::value ? 0 : 2) + (G == 2 ? 0 : 1);
+    auto kern = fwd_pipe_kernel<T, G, UNROLL, MAXT>;
+    const int ti = (std::is_same<T, float>::value ? 0 : 8) + (G == 2 ? 0 : 4) + (UNROLL == 2 ? 0 : 2) +
+                   (MAXT == 1024 ? 0 : (MAXT == 768 ? 1 : 0));
     if (dev >= 0 && dev < 64 && g_fwd_smem_set[ti][dev] < pl.smem) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_pipe_kernel<T, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
         g_fwd_smem_set[ti][dev] = pl.smem;
     }
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
-                 a.B * a.tab->H * pl.qsplit, pl.stages, pl.groups, pl.gwarps, (uint32_t)pl.stage_bytes};
-    fwd_pipe_kernel<T, G><<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
+                 a.B * a.tab->H * pl.qsplit, pl.stages, pl.groups, pl.gwarps, (uint32_t)pl.stage_bytes,
+                 pl.prefetch};
+    kern<<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
     count_launches(1);
     return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t fwd_resident_dispatch(const FwdArgs &a, const ResidentPlan &pl) {
+    if (pl.lanes == 4) return pl.unroll == 2 ? fwd_resident<T, 4, 2, 1024>(a, pl) : fwd_resident<T, 4, 1, 1024>(a, pl);
+    if (pl.maxt == 768) return pl.unroll == 2 ? fwd_resident<T, 2, 2, 768>(a, pl) : fwd_resident<T, 2, 1, 768>(a, pl);
+    return pl.unroll == 2 ? fwd_resident<T, 2, 2, 512>(a, pl) : fwd_resident<T, 2, 1, 512>(a, pl);
 }
 
 // Plan of the resident backward: the whole head's Q, K, V, dO in one stage,
@@ -637,6 +659,9 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     if (stages < 1) return false;
     const int rounds = (N + R - 1) / R;
     pl->lanes = G;
+    pl->unroll = 1;
+    pl->maxt = maxt;
+    pl->prefetch = 0;
     pl->qsplit = 1;
     pl->chunk = N;
     pl->kv_cap = N;
@@ -675,9 +700,7 @@ cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
 }
 
 cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
-    if (a.dtype == FIBATT_F32)
-        return pl.lanes == 2 ? fwd_resident<float, 2>(a, pl) : fwd_resident<float, 4>(a, pl);
-    return pl.lanes == 2 ? fwd_resident<__nv_bfloat16, 2>(a, pl) : fwd_resident<__nv_bfloat16, 4>(a, pl);
+    return a.dtype == FIBATT_F32 ? fwd_resident_dispatch<float>(a, pl) : fwd_resident_dispatch<__nv_bfloat16>(a, pl);
 }
 
 // Read (and optionally clear) the device error word of the current device.
