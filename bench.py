@@ -85,6 +85,12 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def whole_job_value(units_per_rank: int, steps: int, world: int, max_elapsed_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (each rank runs its own batch; weak scaling)."""
+    return world * units_per_rank * steps / (max_elapsed_ms / 1e3)
+
+
 def algorithmic_bytes(wl, backward: bool) -> int:
     """Minimum HBM bytes of one call: every input row read once, every output
     row written once (Q,K,V -> O,LSE forward; Q,K,V,O,dO,LSE -> dQ,dK,dV backward)."""
@@ -342,7 +348,7 @@ def gb300_arm(args):
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
     ms_step = elapsed_ms / K
-    value = world * step.pairs * K / (elapsed_ms / 1e3)
+    value = whole_job_value(step.pairs, K, world, elapsed_ms)
     peak, peak_kind = measured_peaks()
     fb, bb = algorithmic_bytes(wl, False), algorithmic_bytes(wl, True)
     fwd_gbs, bwd_gbs = fb / fwd_ms / 1e6, bb / bwd_ms / 1e6
