@@ -222,6 +222,14 @@ fibatt_status cuda_error(cudaError_t e, const char *what) {
     return set_error(FIBATT_ERR_CUDA, fmt("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e)));
 }
 
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("FIBATT_PDL");
+        return !(e && std::atoi(e) == 0);
+    }();
+    return on;
+}
+
 }  // namespace fibatt
 
 using namespace fibatt;

@@ -12,6 +12,13 @@ constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 constexpr unsigned kFullMask = 0xffffffffu;
 
+// Programmatic dependent launch (sm_90+).  launch_dependents lets the next
+// kernel of the stream be scheduled while this one runs (its blocks take SMs
+// as ours retire); wait blocks until every prerequisite grid has completed
+// and its memory is visible.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // bf16 -> fp32 is exact: the 16 bits are the high half of the fp32 pattern.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

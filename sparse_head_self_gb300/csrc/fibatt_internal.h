@@ -4,9 +4,10 @@
 
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
-#include <cuda_runtime_api.h>
+#include <cuda_runtime.h>
 
 #include "fibatt.h"
 
@@ -101,6 +102,27 @@ struct PlanCache;
 bool cached_plan(const void *support, bool backward, const TableArg &tab, int B, fibatt_dtype dt,
                  ResidentPlan *pl);
 void forget_plans(const void *support);
+
+// Launch `kern` on `stream`; with pdl set, as a programmatic dependent launch
+// (the kernel calls grid_dep_wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Programmatic dependent launches on (FIBATT_PDL unset or non-zero) or off.
+bool pdl_enabled();
 
 cudaError_t launch_fwd_generic(const FwdArgs &a);
 cudaError_t launch_bwd_generic(const BwdArgs &a);

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kThreads)
 fwd_generic_kernel(const __grid_constant__ TableArg tab, const T *__restrict__ Q,
                    const T *__restrict__ K, const T *__restrict__ V, float scale_log2,
                    T *__restrict__ O, float *__restrict__ LSE) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int N = tab.N;
     const int bh = blockIdx.x;
     const int h = bh % tab.H;
@@ -85,6 +87,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 rowdot_kernel(int64_t rows, const T *__restrict__ O, const T *__restrict__ dO,
               float *__restrict__ Dout) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int64_t r = (int64_t)blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;
     const int sub = threadIdx.x % kLanes;
     const int64_t rc = r < rows ? r : rows - 1;
@@ -105,6 +109,8 @@ dq_generic_kernel(const __grid_constant__ TableArg tab, const T *__restrict__ Q,
                   const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ dO,
                   const float *__restrict__ LSE, const float *__restrict__ Dws, float scale,
                   float scale_log2, T *__restrict__ dQ) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int N = tab.N;
     const int bh = blockIdx.x;
     const int h = bh % tab.H;
@@ -162,6 +168,8 @@ dkv_generic_kernel(const __grid_constant__ TableArg tab, const T *__restrict__ Q
                    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ dO,
                    const float *__restrict__ LSE, const float *__restrict__ Dws, float scale,
                    float scale_log2, T *__restrict__ dK, T *__restrict__ dV) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int N = tab.N;
     const int bh = blockIdx.x;
     const int h = bh % tab.H;
@@ -217,36 +225,38 @@ template <typename T>
 cudaError_t fwd_generic(const FwdArgs &a) {
     const TableArg &tab = *a.tab;
     dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + kRowsPerBlock - 1) / kRowsPerBlock));
-    fwd_generic_kernel<T><<<grid, kThreads, 0, a.stream>>>(
-        tab, static_cast<const T *>(a.Q), static_cast<const T *>(a.K),
-        static_cast<const T *>(a.V), a.scale * kLog2e, static_cast<T *>(a.O), a.LSE);
+    const cudaError_t e = launch_kernel(fwd_generic_kernel<T>, grid, dim3(kThreads), 0, a.stream, pdl_enabled(), tab,
+                                        static_cast<const T *>(a.Q), static_cast<const T *>(a.K),
+                                        static_cast<const T *>(a.V), a.scale * kLog2e, static_cast<T *>(a.O), a.LSE);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t bwd_generic(const BwdArgs &a) {
     const TableArg &tab = *a.tab;
     const int64_t rows = (int64_t)a.B * tab.H * tab.N;
-    rowdot_kernel<T><<<(unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock), kThreads, 0,
-                       a.stream>>>(rows, static_cast<const T *>(a.O),
-                                   static_cast<const T *>(a.dO), a.Dws);
-    cudaError_t e = cudaGetLastError();
+    const bool pdl = pdl_enabled();
+    cudaError_t e = launch_kernel(rowdot_kernel<T>, dim3((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock)),
+                                  dim3(kThreads), 0, a.stream, pdl, rows, static_cast<const T *>(a.O),
+                                  static_cast<const T *>(a.dO), a.Dws);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + kRowsPerBlock - 1) / kRowsPerBlock));
     const float sl2 = a.scale * kLog2e;
-    dq_generic_kernel<T><<<grid, kThreads, 0, a.stream>>>(
-        tab, static_cast<const T *>(a.Q), static_cast<const T *>(a.K),
-        static_cast<const T *>(a.V), static_cast<const T *>(a.dO), a.LSE, a.Dws, a.scale, sl2,
-        static_cast<T *>(a.dQ));
-    e = cudaGetLastError();
+    e = launch_kernel(dq_generic_kernel<T>, grid, dim3(kThreads), 0, a.stream, pdl, tab, static_cast<const T *>(a.Q),
+                      static_cast<const T *>(a.K), static_cast<const T *>(a.V), static_cast<const T *>(a.dO),
+                      static_cast<const float *>(a.LSE), static_cast<const float *>(a.Dws), a.scale, sl2,
+                      static_cast<T *>(a.dQ));
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dkv_generic_kernel<T><<<grid, kThreads, 0, a.stream>>>(
-        tab, static_cast<const T *>(a.Q), static_cast<const T *>(a.K),
-        static_cast<const T *>(a.V), static_cast<const T *>(a.dO), a.LSE, a.Dws, a.scale, sl2,
-        static_cast<T *>(a.dK), static_cast<T *>(a.dV));
+    e = launch_kernel(dkv_generic_kernel<T>, grid, dim3(kThreads), 0, a.stream, pdl, tab,
+                      static_cast<const T *>(a.Q), static_cast<const T *>(a.K), static_cast<const T *>(a.V),
+                      static_cast<const T *>(a.dO), static_cast<const float *>(a.LSE),
+                      static_cast<const float *>(a.Dws), a.scale, sl2, static_cast<T *>(a.dK),
+                      static_cast<T *>(a.dV));
     count_launches(3);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -248,6 +248,10 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         }
     }
     __syncthreads();
+    // let the next kernel of the stream take SMs as this grid retires, and
+    // touch no global memory before the previous kernel has completed
+    grid_dep_launch();
+    grid_dep_wait();
 
     const size_t q_off = 0, k_off = (size_t)p.chunk * RB, v_off = k_off + (size_t)p.kv_cap * RB;
     if (warp == 0) {
@@ -411,6 +415,8 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         }
     }
     __syncthreads();
+    grid_dep_launch();
+    grid_dep_wait();
     const size_t tens = (size_t)N * RB;   // one tensor's rows in a stage: Q | K | V | dO
     if (warp == 0) {
         if (lane != 0) return;
@@ -626,9 +632,10 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
                  a.B * a.tab->H * pl.qsplit, pl.stages, pl.groups, pl.gwarps, (uint32_t)pl.stage_bytes,
                  pl.prefetch};
-    kern<<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
+    const cudaError_t e =
+        launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>
@@ -690,9 +697,10 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 a.B * a.tab->H, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
                 (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count)};
-    kern<<<pl.grid, pl.threads, pl.smem, a.stream>>>(*a.tab, p);
+    const cudaError_t e =
+        launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {

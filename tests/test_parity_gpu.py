@@ -191,6 +191,38 @@ def test_side_stream_and_repeatability():
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
 
 
+@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
+def test_chained_calls_match_synchronised_calls(kernel_path):
+    """Launches are programmatic dependent launches: each kernel may start
+    while the previous one drains.  A chain that reuses its buffers (fwd
+    writes O while the previous bwd still reads it, and so on) must give
+    what the same calls give with a synchronisation between each."""
+    wl = WORKLOADS["vitb"].with_batch(4)
+    sup = support_for(wl)
+    inputs = [to_dev(*make_inputs(wl, 60 + i)) for i in range(3)]
+    ref = []
+    for qd, kd, vd, dod in inputs:
+        O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+        torch.cuda.synchronize()
+        dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+        torch.cuda.synchronize()
+        ref.append([t.clone() for t in (O, L, dQ, dK, dV)])
+    # one O / LSE for the whole chain (the next fwd overwrites what the
+    # previous bwd reads); gradients of each call kept apart
+    O = torch.empty_like(inputs[0][0])
+    L = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device="cuda")
+    grads = [[torch.empty_like(O) for _ in range(3)] for _ in range(6)]
+    for i in range(6):
+        qd, kd, vd, dod = inputs[i % 3]
+        api.fwd(sup, qd, kd, vd, wl.scale, O=O, LSE=L)
+        api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale, dQ=grads[i][0], dK=grads[i][1], dV=grads[i][2])
+    torch.cuda.synchronize()
+    assert torch.equal(O, ref[2][0]) and torch.equal(L, ref[2][1])
+    for i in range(6):
+        for a, b in zip(grads[i], ref[i % 3][2:]):
+            assert torch.equal(a, b)
+
+
 # ----------------------------------------------- full sizes, bench launches
 
 @pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
