@@ -135,8 +135,12 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype,
                          const void *Q, const void *K, const void *V, float scale,
                          void *O, float *LSE, cudaStream_t stream);
 
-/* Device scratch the backward pass needs for B batches of this support, in
- * bytes (one fp32 per query row: D_j = <dO_j, O_j>). */
+/* Device scratch the backward pass may need for B batches of this support,
+ * in bytes: the larger of one fp32 per query row (D_j = <dO_j, O_j>, global-
+ * memory kernels) and the pair weights P and dS of every attended pair
+ * (2 x the largest per-head table x N fp32 per (b, h); kernels for windows
+ * too wide for shared memory).  The shared-memory-resident kernels touch
+ * none of it. */
 size_t fibatt_bwd_workspace_bytes(fibatt_support_t s, int B);
 
 /* Backward pass for the loss whose gradient with respect to O is dO:

@@ -59,12 +59,13 @@ int64_t floor_phi(int64_t n) { return n <= 0 ? 0 : (n + int_sqrt(5 * n * n)) / 2
 
 // Kernel family override for tests and tuning: FIBATT_PATH=generic forces the
 // generic kernels, FIBATT_PATH=resident forbids falling back to them.
-enum class PathSel { Auto, Generic, Resident };
+enum class PathSel { Auto, Generic, Resident, Flat };
 PathSel path_sel() {
     const char *e = std::getenv("FIBATT_PATH");
     if (!e) return PathSel::Auto;
     if (std::strcmp(e, "generic") == 0) return PathSel::Generic;
     if (std::strcmp(e, "resident") == 0) return PathSel::Resident;
+    if (std::strcmp(e, "flat") == 0) return PathSel::Flat;
     return PathSel::Auto;
 }
 
@@ -163,7 +164,7 @@ std::map<PlanKey, PlanEntry> g_plans;
 std::string tuning_env() {
     std::string r;
     for (const char *n : {"FIBATT_QSPLIT", "FIBATT_LANES", "FIBATT_GROUPS", "FIBATT_STAGES", "FIBATT_BWD_THREADS",
-                          "FIBATT_UNROLL", "FIBATT_FWD_THREADS", "FIBATT_PREFETCH"}) {
+                          "FIBATT_UNROLL", "FIBATT_FWD_THREADS", "FIBATT_PREFETCH", "FIBATT_BWD_LANES"}) {
         const char *e = std::getenv(n);
         r += e ? e : "-";
         r += ',';
@@ -354,12 +355,14 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     const PathSel sel = path_sel();
     ResidentPlan pl;
     cudaError_t e;
-    if (sel != PathSel::Generic && cached_plan(s, false, s->impl.tab, B, dtype, &pl)) {
+    if (sel == PathSel::Generic) {
+        e = launch_fwd_generic(a);
+    } else if (sel != PathSel::Flat && cached_plan(s, false, s->impl.tab, B, dtype, &pl)) {
         e = launch_fwd_resident(a, pl);
     } else {
         if (sel == PathSel::Resident)
             return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: windows do not fit in shared memory");
-        e = launch_fwd_generic(a);
+        e = launch_fwd_flat(a);
     }
     if (e != cudaSuccess) return cuda_error(e, "fibatt_fwd launch");
     return FIBATT_OK;
@@ -368,14 +371,27 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
 size_t fibatt_bwd_workspace_bytes(fibatt_support_t s, int B) {
     if (!s || B < 1) return 0;
     const size_t rows = (size_t)B * s->impl.tab.H * s->impl.tab.N;
-    return (rows * sizeof(float) + 255) / 256 * 256;
+    const size_t bytes = std::max(rows * sizeof(float), flat_bwd_scratch_bytes(s->impl.tab, B));
+    return (bytes + 255) / 256 * 256;
 }
 
-// Workspace the chosen backward path actually touches (0 for the resident
-// kernel, which keeps its scratch in shared memory).
-static size_t bwd_workspace_needed(fibatt_support_t s, int B, fibatt_dtype dt, bool *resident, ResidentPlan *pl) {
-    *resident = path_sel() != PathSel::Generic && cached_plan(s, true, s->impl.tab, B, dt, pl);
-    return *resident ? 0 : fibatt_bwd_workspace_bytes(s, B);
+enum class BwdPath { Resident, Flat, Generic };
+
+// The backward path and the workspace it actually touches (0 for the
+// resident kernel, which keeps its scratch in shared memory).
+static size_t bwd_workspace_needed(fibatt_support_t s, int B, fibatt_dtype dt, BwdPath *path, ResidentPlan *pl) {
+    const PathSel sel = path_sel();
+    const TableArg &tab = s->impl.tab;
+    if (sel == PathSel::Generic) {
+        *path = BwdPath::Generic;
+        return (size_t)B * tab.H * tab.N * sizeof(float);
+    }
+    if (sel != PathSel::Flat && cached_plan(s, true, tab, B, dt, pl)) {
+        *path = BwdPath::Resident;
+        return 0;
+    }
+    *path = BwdPath::Flat;
+    return flat_bwd_scratch_bytes(tab, B);
 }
 
 fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
@@ -388,10 +404,10 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
         (st = check_tensor(dK, "dK")) || (st = check_tensor(dV, "dV")))
         return st;
     if (!LSE || !aligned(LSE, 4)) return set_error(FIBATT_ERR_INVALID_ARG, "LSE is NULL or misaligned");
-    bool resident = false;
+    BwdPath path = BwdPath::Generic;
     ResidentPlan pl;
-    const size_t need = bwd_workspace_needed(s, B, dtype, &resident, &pl);
-    if (!resident && path_sel() == PathSel::Resident)
+    const size_t need = bwd_workspace_needed(s, B, dtype, &path, &pl);
+    if (path != BwdPath::Resident && path_sel() == PathSel::Resident)
         return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: the backward does not fit in shared memory");
     if (need > 0) {
         if ((st = check_tensor(workspace, "workspace"))) return st;
@@ -402,7 +418,9 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     if (fault("launch")) return set_error(FIBATT_ERR_CUDA, "injected launch failure (FIBATT_FAULT=launch)");
     BwdArgs a{&s->impl.tab, B, dtype, Q, K, V, O, dO, LSE, dQ, dK, dV, static_cast<float *>(workspace),
               scale, stream};
-    cudaError_t e = resident ? launch_bwd_resident(a, pl) : launch_bwd_generic(a);
+    cudaError_t e = path == BwdPath::Resident ? launch_bwd_resident(a, pl)
+                    : path == BwdPath::Flat   ? launch_bwd_flat(a)
+                                              : launch_bwd_generic(a);
     if (e != cudaSuccess) return cuda_error(e, "fibatt_bwd launch");
     return FIBATT_OK;
 }

@@ -70,7 +70,7 @@ struct BwdArgs {
     const void *Q, *K, *V, *O, *dO;
     const float *LSE;
     void *dQ, *dK, *dV;
-    float *Dws;                        // [B*H*N] fp32 scratch (generic path)
+    float *Dws;                        // fp32 scratch: [B*H*N] (generic) or pair weights (flat)
     float scale;
     cudaStream_t stream;
 };
@@ -127,6 +127,9 @@ bool pdl_enabled();
 cudaError_t launch_fwd_generic(const FwdArgs &a);
 cudaError_t launch_bwd_generic(const BwdArgs &a);
 cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl);
+cudaError_t launch_fwd_flat(const FwdArgs &a);
+cudaError_t launch_bwd_flat(const BwdArgs &a);       // a.Dws: pair-weight scratch
+size_t flat_bwd_scratch_bytes(const TableArg &tab, int B);
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
 

@@ -116,7 +116,7 @@ constexpr float kMaxInit = -1.0e30f;
 // triggers.  Two offsets per step so their shared-memory loads overlap.
 template <typename T, int G, int UNROLL>
 __device__ __forceinline__ void fwd_offsets(const int *off, int N, int tb, int te, int j, bool valid, int lo,
-                                            int nrows, const uint8_t *sK, int vdelta, const Slice<T, G> &q,
+                                            int nrows, const uint8_t *sK, ptrdiff_t vdelta, const Slice<T, G> &q,
                                             const LaneGeom<T, G> &lg, float sl2, SoftmaxState<G> &st) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
@@ -180,7 +180,7 @@ __device__ __forceinline__ void round_range(const int *off, int N, int t0, int t
 // Round r of a unit: query rows [q0 + r R, q0 + r R + R) with R = 32 / G.
 template <typename T, int G, int UNROLL>
 __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, const PipeParams &p, const Unit &g,
-                                          const uint8_t *sQ, const uint8_t *sK, int vdelta, int r,
+                                          const uint8_t *sQ, const uint8_t *sK, ptrdiff_t vdelta, int r,
                                           const LaneGeom<T, G> &lg) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
@@ -304,10 +304,49 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const Unit g = unit_geometry(tab, p, u);
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         for (int r = wg; r < rpu; r += p.gwarps)
-            fwd_round<T, G, UNROLL>(tab, s_off, p, g, st + q_off, st + k_off, (int)(v_off - k_off), r, lg);
+            fwd_round<T, G, UNROLL>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
+}
+
+// ------------------------------------------------------------ flat forward
+//
+// The same rounds with nothing staged: the query, key and value rows are read
+// from global memory (L1/L2) at the addresses the round would have used in
+// shared memory.  For heads whose key windows do not fit in shared memory
+// (long sequences with wide windows).  Block: kFlatWarps warps of one
+// (b, h); warp w of block y takes round y * kFlatWarps + w.
+constexpr int kFlatWarps = 8;
+
+template <typename T, int G, int UNROLL>
+__global__ void __launch_bounds__(kFlatWarps * 32)
+fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
+    __shared__ int s_off[kMaxEntries];
+    constexpr int RB = Slice<T, G>::kRowBytes;
+    const int N = tab.N;
+    const int bh = blockIdx.x, h = bh % tab.H;
+    const int t0 = tab.start[h], t1 = tab.start[h + 1];
+    for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
+    __syncthreads();
+    grid_dep_launch();
+    grid_dep_wait();
+    Unit g;
+    g.bh = bh;
+    g.h = h;
+    g.q0 = 0;
+    g.q1 = N;
+    g.t0 = t0;
+    g.t1 = t1;
+    g.lo = 0;
+    g.nrows = t1 > t0 ? N : 0;
+    const size_t row0 = (size_t)bh * N * RB;
+    const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0;
+    const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0;
+    const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
+    const LaneGeom<T, G> lg;
+    const int r = blockIdx.y * kFlatWarps + (threadIdx.x >> 5);
+    fwd_round<T, G, UNROLL>(tab, s_off, p, g, gQ, gK, vdelta, r, lg);
 }
 
 // ---------------------------------------------------------------- backward
@@ -343,7 +382,7 @@ struct BwdParams {
 // in-range pairs are written to the scratch.
 template <typename T, int G>
 __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int tb, int te, int j, bool valid,
-                                              const uint8_t *sK, int vdelta, const Slice<T, G> &q,
+                                              const uint8_t *sK, ptrdiff_t vdelta, const Slice<T, G> &q,
                                               const Slice<T, G> &g, float Dj, float lse2, float sl2,
                                               const LaneGeom<T, G> &lg, float *scrP, float *scrS,
                                               float2 (&dq)[32 / G]) {
@@ -373,7 +412,7 @@ __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int
 // into [0, N) and an out-of-range pair contributes P = dS = 0.
 template <typename T, int G>
 __device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int t1, int tb, int te, int k,
-                                              bool valid, const uint8_t *sQ, int gdelta,
+                                              bool valid, const uint8_t *sQ, ptrdiff_t gdelta,
                                               const LaneGeom<T, G> &lg, const float *scrP, const float *scrS,
                                               float2 (&dk)[32 / G], float2 (&dv)[32 / G]) {
     using S = Slice<T, G>;
@@ -474,7 +513,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             float2 dq[32 / G];
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
-            bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (int)tens, q, g, Dj, lse2, p.scale_log2, lg,
+            bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg,
                                 scrP, scrS, dq);
             if (valid) {
 #pragma unroll
@@ -494,7 +533,8 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             float2 dk[32 / G], dv[32 / G];
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
-            bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (int)(3 * tens), lg, scrP, scrS, dk, dv);
+            bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (ptrdiff_t)(3 * tens), lg, scrP, scrS, dk,
+                                dv);
             if (valid) {
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
@@ -507,11 +547,105 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     }
 }
 
+// ------------------------------------------------------------ flat backward
+//
+// The two phases as two kernels over rows read from global memory, with the
+// pair weights P and dS in a global scratch [b, h][2][max_count][N] (phase A
+// writes the pairs in range, phase B reads exactly those).  Phase A: dQ;
+// phase B: dK, dV.  Block: kFlatWarps warps of one (b, h), one round each.
+template <typename T, int G>
+__global__ void __launch_bounds__(kFlatWarps * 32)
+bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float *scr) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
+    __shared__ int s_off[kMaxEntries];
+    const int N = tab.N;
+    const int bh = blockIdx.x, h = bh % tab.H;
+    const int t0 = tab.start[h], t1 = tab.start[h + 1];
+    for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
+    __syncthreads();
+    grid_dep_launch();
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.y * kFlatWarps + (threadIdx.x >> 5);
+    if (r * R >= N) return;
+    const size_t row0 = (size_t)bh * N;
+    const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB;
+    const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
+    float *scrP = scr + (size_t)bh * 2 * p.max_count * N;
+    float *scrS = scrP + (size_t)p.max_count * N;
+    const LaneGeom<T, G> lg;
+    const int jl = r * R + lane / G;
+    const bool valid = jl < N;
+    const int j = valid ? jl : N - 1;
+    const int jfirst = r * R, jlast = min(N, r * R + R) - 1;
+    int tb = t0, te = t0;
+    if (t1 > t0) round_range(s_off, N, t0, t1, jfirst, jlast, tb, te);
+    S q, g, o;
+    q.load_global(static_cast<const T *>(p.Q) + (row0 + j) * kHeadDim, lg.c);
+    g.load_global(static_cast<const T *>(p.dO) + (row0 + j) * kHeadDim, lg.c);
+    o.load_global(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim, lg.c);
+    const float Dj = group_sum<G>(g.dot(o));
+    const float lse2 = p.LSE[row0 + j] * kLog2e;
+    float2 dq[32 / G];
+#pragma unroll
+    for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
+    bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, scrP, scrS,
+                        dq);
+    if (valid) {
+#pragma unroll
+        for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
+        S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
+    }
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kFlatWarps * 32)
+bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const float *scr) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
+    __shared__ int s_off[kMaxEntries];
+    const int N = tab.N;
+    const int bh = blockIdx.x, h = bh % tab.H;
+    const int t0 = tab.start[h], t1 = tab.start[h + 1];
+    for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
+    __syncthreads();
+    grid_dep_launch();
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.y * kFlatWarps + (threadIdx.x >> 5);
+    if (r * R >= N) return;
+    const size_t row0 = (size_t)bh * N;
+    const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB;
+    const ptrdiff_t gdelta = static_cast<const uint8_t *>(p.dO) - static_cast<const uint8_t *>(p.Q);
+    const float *scrP = scr + (size_t)bh * 2 * p.max_count * N;
+    const float *scrS = scrP + (size_t)p.max_count * N;
+    const LaneGeom<T, G> lg;
+    const int kl = r * R + lane / G;
+    const bool valid = kl < N;
+    const int k = valid ? kl : N - 1;
+    const int kfirst = r * R, klast = min(N, r * R + R) - 1;
+    int tb = t0, te = t0;
+    if (t1 > t0) round_range(s_off, N, t0, t1, kfirst, klast, tb, te);
+    float2 dk[32 / G], dv[32 / G];
+#pragma unroll
+    for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
+    bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, gQ, gdelta, lg, scrP, scrS, dk, dv);
+    if (valid) {
+#pragma unroll
+        for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
+        S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
+        S::store(static_cast<T *>(p.dV) + (row0 + k) * kHeadDim, lg.c, dv);
+    }
+}
+
 size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
 
 int g_sm_count[64] = {0};
 size_t g_fwd_smem_set[16][64] = {{0}};
-size_t g_bwd_smem_set[4][64] = {{0}};
+size_t g_bwd_smem_set[8][64] = {{0}};
 
 int sm_count(int dev) {
     if (dev < 0 || dev >= 64) return 148;
@@ -655,9 +789,15 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     int dev = 0;
     cudaGetDevice(&dev);
     const int sms = sm_count(dev);
-    const int G = 4, R = 32 / G;
+    // two lanes per row for bf16 (fewer shuffles and less per-pair scalar
+    // work than four; measured faster), four for fp32 rows (two would spill)
+    int G = dt == FIBATT_F32 ? 4 : 2;
+    if (const char *e = getenv("FIBATT_BWD_LANES")) G = atoi(e) == 2 ? 2 : 4;
+    if (dt == FIBATT_F32) G = 4;
+    const int R = 32 / G;
     int maxt = 512;
     if (const char *e = getenv("FIBATT_BWD_THREADS")) maxt = atoi(e) == 1024 ? 1024 : 512;
+    if (G == 2) maxt = 512;
     const int maxw = maxt / 32;
     const size_t stage = (4 * (size_t)N * RB + 127) / 128 * 128;
     const size_t scratch = (2 * (size_t)std::max(1, tab.max_count) * N * 4 + 127) / 128 * 128;
@@ -687,8 +827,9 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     int dev = 0;
     cudaGetDevice(&dev);
     const int ti = std::is_same<T, float>::value ? 0 : 1;
-    auto kern = pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>;
-    const int ki = ti * 2 + (pl.threads > 512 ? 1 : 0);
+    auto kern = pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512>
+                              : (pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>);
+    const int ki = ti * 4 + (pl.lanes == 2 ? 2 : (pl.threads > 512 ? 1 : 0));
     if (dev >= 0 && dev < 64 && g_bwd_smem_set[ki][dev] < pl.smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
@@ -703,8 +844,62 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <typename T, int G>
+static cudaError_t bwd_flat(const BwdArgs &a) {
+    constexpr int R = 32 / G;
+    const TableArg &tab = *a.tab;
+    BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
+                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count)};
+    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * kFlatWarps - 1) / (R * kFlatWarps)));
+    const bool pdl = pdl_enabled();
+    cudaError_t e = launch_kernel(bwd_flat_a_kernel<T, G>, grid, dim3(kFlatWarps * 32), 0, a.stream, pdl, tab, p,
+                                  a.Dws);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_kernel(bwd_flat_b_kernel<T, G>, grid, dim3(kFlatWarps * 32), 0, a.stream, pdl, tab, p,
+                      static_cast<const float *>(a.Dws));
+    count_launches(2);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_bwd_flat(const BwdArgs &a) {
+    int G = 4;
+    if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
+    if (a.dtype == FIBATT_F32) return bwd_flat<float, 4>(a);
+    return G == 2 ? bwd_flat<__nv_bfloat16, 2>(a) : bwd_flat<__nv_bfloat16, 4>(a);
+}
+
+size_t flat_bwd_scratch_bytes(const TableArg &tab, int B) {
+    return (size_t)B * tab.H * 2 * std::max(1, (int)tab.max_count) * tab.N * sizeof(float);
+}
+
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     return a.dtype == FIBATT_F32 ? bwd_resident<float>(a, pl) : bwd_resident<__nv_bfloat16>(a, pl);
+}
+
+template <typename T, int G>
+static cudaError_t fwd_flat(const FwdArgs &a) {
+    constexpr int R = 32 / G;
+    const TableArg &tab = *a.tab;
+    PipeParams p{};
+    p.Q = a.Q;
+    p.K = a.K;
+    p.V = a.V;
+    p.O = a.O;
+    p.LSE = a.LSE;
+    p.scale_log2 = a.scale * kLog2e;
+    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * kFlatWarps - 1) / (R * kFlatWarps)));
+    const cudaError_t e = launch_kernel(fwd_flat_kernel<T, G, 2>, grid, dim3(kFlatWarps * 32), 0, a.stream,
+                                        pdl_enabled(), tab, p);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_fwd_flat(const FwdArgs &a) {
+    int G = 4;   // four lanes per row: more warps in flight to cover global-load latency (measured faster)
+    if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
+    if (a.dtype == FIBATT_F32) return G == 4 ? fwd_flat<float, 4>(a) : fwd_flat<float, 2>(a);
+    return G == 4 ? fwd_flat<__nv_bfloat16, 4>(a) : fwd_flat<__nv_bfloat16, 2>(a);
 }
 
 cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {

@@ -22,7 +22,10 @@ oracle.set_threads(oracle.max_threads())
 
 @pytest.fixture
 def kernel_path(request, monkeypatch):
-    """Select the kernel family through FIBATT_PATH for one test."""
+    """Select the kernel family through FIBATT_PATH for one test: generic
+    (global-memory kernels), resident (shared-memory staged), flat (the
+    resident arithmetic on rows read from global memory; backward generic)
+    or auto (the library's choice)."""
     path = getattr(request, "param", "auto")
     if path == "auto":
         monkeypatch.delenv("FIBATT_PATH", raising=False)
@@ -54,16 +57,17 @@ def _bwd_full(wl, seed=0):
 
 # ------------------------------------------------------------ small, full
 
-@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 def test_tiny_fwd_fp32_full(kernel_path):
     _fwd_full(WORKLOADS["tiny"])
 
 
-def test_tiny_bwd_fp32_full():
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
+def test_tiny_bwd_fp32_full(kernel_path):
     _bwd_full(WORKLOADS["tiny"])
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 @pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_vitb_shape_small_batch_full(name, dtype, kernel_path):
@@ -77,7 +81,25 @@ def test_video_shape_one_batch_fwd_full():
     _fwd_full(wl, seed=7)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat"], indirect=True)
+def test_video_shape_two_heads_bwd_full(kernel_path):
+    # every row of two heads (the narrowest and the widest window) of one
+    # batch element: every gradient compared with the oracle's
+    wl = WORKLOADS["video"].with_batch(1)
+    q, k, v, do = make_inputs(wl, 9)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    heads = oracle_heads(wl)
+    for h in (0, wl.H - 1):
+        rQ, rK, rV = oracle.bwd_head(q[0, h], k[0, h], v[0, h], do[0, h], heads[h], wl.scale)
+        assert_close(f"video h{h} dQ", dQ[0, h].float().cpu(), rQ, wl.dtype)
+        assert_close(f"video h{h} dK", dK[0, h].float().cpu(), rK, wl.dtype)
+        assert_close(f"video h{h} dV", dV[0, h].float().cpu(), rV, wl.dtype)
+
+
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "auto"], indirect=True)
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 63, 64, 65, 127, 129, 300])
 @pytest.mark.parametrize("diag", [False, True])
 def test_edge_sizes(N, diag, kernel_path):
@@ -99,7 +121,7 @@ def test_resident_query_chunks(qsplit, dtype, monkeypatch):
     _fwd_full(wl, seed=23)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 def test_empty_support_rows_are_zero(kernel_path):
     # N = 3, row 2 of the Wythoff array (4, 7), no diagonal: no pair at all
     N = 3
@@ -111,7 +133,7 @@ def test_empty_support_rows_are_zero(kernel_path):
     assert torch.all(dQ == 0) and torch.all(dK == 0) and torch.all(dV == 0)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "resident"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 def test_diagonal_only_support_returns_V(kernel_path):
     N = 77
     sup = api.Support.from_distances(N, [[], []], True)
@@ -123,7 +145,7 @@ def test_diagonal_only_support_returns_V(kernel_path):
     assert (L.double() - ref).abs().max().item() <= 1e-5
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "auto"], indirect=True)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_dense_support_equals_softmax_attention(dtype, kernel_path):
     # every distance 0..N-1: plain softmax attention (checked against the oracle,
@@ -144,7 +166,7 @@ def test_dense_support_equals_softmax_attention(dtype, kernel_path):
         assert_close(f"dense {n}", g.float().cpu(), r, dtype)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "auto"], indirect=True)
 def test_modified_wythoff_variant(kernel_path):
     wl = WORKLOADS["tiny"]
     q, k, v, do = make_inputs(wl, 13)
@@ -191,7 +213,7 @@ def test_side_stream_and_repeatability():
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "auto"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "auto"], indirect=True)
 def test_chained_calls_match_synchronised_calls(kernel_path):
     """Launches are programmatic dependent launches: each kernel may start
     while the previous one drains.  A chain that reuses its buffers (fwd
