@@ -317,10 +317,10 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
 // shared memory.  For heads whose key windows do not fit in shared memory
 // (long sequences with wide windows).  Block: kFlatWarps warps of one
 // (b, h); warp w of block y takes round y * kFlatWarps + w.
-constexpr int kFlatWarps = 8;
+constexpr int kFlatWarps = 4;   // 128-thread blocks measured fastest (4 to 32 warps tried)
 
-template <typename T, int G, int UNROLL>
-__global__ void __launch_bounds__(kFlatWarps * 32)
+template <typename T, int G, int UNROLL, int W = kFlatWarps>
+__global__ void __launch_bounds__(W * 32)
 fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     __shared__ int s_off[kMaxEntries];
     constexpr int RB = Slice<T, G>::kRowBytes;
@@ -345,7 +345,7 @@ fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0;
     const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
     const LaneGeom<T, G> lg;
-    const int r = blockIdx.y * kFlatWarps + (threadIdx.x >> 5);
+    const int r = blockIdx.y * W + (threadIdx.x >> 5);
     fwd_round<T, G, UNROLL>(tab, s_off, p, g, gQ, gK, vdelta, r, lg);
 }
 
@@ -553,8 +553,8 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 // pair weights P and dS in a global scratch [b, h][2][max_count][N] (phase A
 // writes the pairs in range, phase B reads exactly those).  Phase A: dQ;
 // phase B: dK, dV.  Block: kFlatWarps warps of one (b, h), one round each.
-template <typename T, int G>
-__global__ void __launch_bounds__(kFlatWarps * 32)
+template <typename T, int G, int W = kFlatWarps>
+__global__ void __launch_bounds__(W * 32)
 bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float *scr) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
@@ -568,7 +568,7 @@ bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float
     grid_dep_launch();
     grid_dep_wait();
     const int lane = threadIdx.x & 31;
-    const int r = blockIdx.y * kFlatWarps + (threadIdx.x >> 5);
+    const int r = blockIdx.y * W + (threadIdx.x >> 5);
     if (r * R >= N) return;
     const size_t row0 = (size_t)bh * N;
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB;
@@ -600,8 +600,8 @@ bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float
     }
 }
 
-template <typename T, int G>
-__global__ void __launch_bounds__(kFlatWarps * 32)
+template <typename T, int G, int W = kFlatWarps>
+__global__ void __launch_bounds__(W * 32)
 bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const float *scr) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
@@ -615,7 +615,7 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
     grid_dep_launch();
     grid_dep_wait();
     const int lane = threadIdx.x & 31;
-    const int r = blockIdx.y * kFlatWarps + (threadIdx.x >> 5);
+    const int r = blockIdx.y * W + (threadIdx.x >> 5);
     if (r * R >= N) return;
     const size_t row0 = (size_t)bh * N;
     const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB;
@@ -844,19 +844,18 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <typename T, int G>
+template <typename T, int G, int W = kFlatWarps>
 static cudaError_t bwd_flat(const BwdArgs &a) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count)};
-    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * kFlatWarps - 1) / (R * kFlatWarps)));
+    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
-    cudaError_t e = launch_kernel(bwd_flat_a_kernel<T, G>, grid, dim3(kFlatWarps * 32), 0, a.stream, pdl, tab, p,
-                                  a.Dws);
+    cudaError_t e = launch_kernel(bwd_flat_a_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p, a.Dws);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_kernel(bwd_flat_b_kernel<T, G>, grid, dim3(kFlatWarps * 32), 0, a.stream, pdl, tab, p,
+    e = launch_kernel(bwd_flat_b_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p,
                       static_cast<const float *>(a.Dws));
     count_launches(2);
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -877,7 +876,7 @@ cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     return a.dtype == FIBATT_F32 ? bwd_resident<float>(a, pl) : bwd_resident<__nv_bfloat16>(a, pl);
 }
 
-template <typename T, int G>
+template <typename T, int G, int W = kFlatWarps, int U = 2>
 static cudaError_t fwd_flat(const FwdArgs &a) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
@@ -888,8 +887,8 @@ static cudaError_t fwd_flat(const FwdArgs &a) {
     p.O = a.O;
     p.LSE = a.LSE;
     p.scale_log2 = a.scale * kLog2e;
-    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * kFlatWarps - 1) / (R * kFlatWarps)));
-    const cudaError_t e = launch_kernel(fwd_flat_kernel<T, G, 2>, grid, dim3(kFlatWarps * 32), 0, a.stream,
+    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * W - 1) / (R * W)));
+    const cudaError_t e = launch_kernel(fwd_flat_kernel<T, G, U, W>, grid, dim3(W * 32), 0, a.stream,
                                         pdl_enabled(), tab, p);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
