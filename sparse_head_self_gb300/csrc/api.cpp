@@ -418,6 +418,7 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     if (fault("launch")) return set_error(FIBATT_ERR_CUDA, "injected launch failure (FIBATT_FAULT=launch)");
     BwdArgs a{&s->impl.tab, B, dtype, Q, K, V, O, dO, LSE, dQ, dK, dV, static_cast<float *>(workspace),
               scale, stream};
+
     cudaError_t e = path == BwdPath::Resident ? launch_bwd_resident(a, pl)
                     : path == BwdPath::Flat   ? launch_bwd_flat(a)
                                               : launch_bwd_generic(a);

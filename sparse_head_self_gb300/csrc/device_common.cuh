@@ -15,7 +15,9 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // Programmatic dependent launch (sm_90+).  launch_dependents lets the next
 // kernel of the stream be scheduled while this one runs (its blocks take SMs
 // as ours retire); wait blocks until every prerequisite grid has completed
-// and its memory is visible.  Both are no-ops for an ordinary launch.
+// and its memory is visible.  Both are no-ops for an ordinary launch.  The
+// kernels call wait first and launch_dependents after it, so a dependent
+// grid is never scheduled before this grid's own prerequisites are done.
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

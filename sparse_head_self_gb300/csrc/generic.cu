@@ -33,8 +33,8 @@ __global__ void __launch_bounds__(kThreads)
 fwd_generic_kernel(const __grid_constant__ TableArg tab, const T *__restrict__ Q,
                    const T *__restrict__ K, const T *__restrict__ V, float scale_log2,
                    T *__restrict__ O, float *__restrict__ LSE) {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int N = tab.N;
     const int bh = blockIdx.x;
     const int h = bh % tab.H;
@@ -87,8 +87,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 rowdot_kernel(int64_t rows, const T *__restrict__ O, const T *__restrict__ dO,
               float *__restrict__ Dout) {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int64_t r = (int64_t)blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;
     const int sub = threadIdx.x % kLanes;
     const int64_t rc = r < rows ? r : rows - 1;
@@ -109,8 +109,8 @@ dq_generic_kernel(const __grid_constant__ TableArg tab, const T *__restrict__ Q,
                   const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ dO,
                   const float *__restrict__ LSE, const float *__restrict__ Dws, float scale,
                   float scale_log2, T *__restrict__ dQ) {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int N = tab.N;
     const int bh = blockIdx.x;
     const int h = bh % tab.H;
@@ -168,8 +168,8 @@ dkv_generic_kernel(const __grid_constant__ TableArg tab, const T *__restrict__ Q
                    const T *__restrict__ K, const T *__restrict__ V, const T *__restrict__ dO,
                    const float *__restrict__ LSE, const float *__restrict__ Dws, float scale,
                    float scale_log2, T *__restrict__ dK, T *__restrict__ dV) {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int N = tab.N;
     const int bh = blockIdx.x;
     const int h = bh % tab.H;

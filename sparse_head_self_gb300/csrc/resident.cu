@@ -248,10 +248,11 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         }
     }
     __syncthreads();
-    // let the next kernel of the stream take SMs as this grid retires, and
-    // touch no global memory before the previous kernel has completed
-    grid_dep_launch();
+    // touch no global memory before the previous kernel has completed; then
+    // let the next kernel of the stream take SMs as this grid retires (only
+    // after the wait, so a dependent never runs ahead of our prerequisites)
     grid_dep_wait();
+    grid_dep_launch();
 
     const size_t q_off = 0, k_off = (size_t)p.chunk * RB, v_off = k_off + (size_t)p.kv_cap * RB;
     if (warp == 0) {
@@ -329,8 +330,8 @@ fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     const int t0 = tab.start[h], t1 = tab.start[h + 1];
     for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
     __syncthreads();
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     Unit g;
     g.bh = bh;
     g.h = h;
@@ -363,6 +364,41 @@ fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
 //     and the pair's forward offset index is the mirror t0 + t1 - 1 - t';
 //     dK_k = scale * sum dS q_j, dV_k = sum P dO_j -- each key row owned by
 //     one lane group, no atomics.
+
+// <O_j, dO_j> over the full row: O from global memory, dO from shared
+// memory; the lane walks the 16-byte chunks starting at its own index so a
+// warp's lanes (one row each) touch different bank groups.
+__device__ __forceinline__ float row_dot_global_shared(const __nv_bfloat16 *o, const uint8_t *g, int lane) {
+    const uint4 *o4 = reinterpret_cast<const uint4 *>(o);
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int cc = (c + lane) & 7;
+        const uint4 x = __ldg(o4 + cc);
+        const uint4 y = *reinterpret_cast<const uint4 *>(g + 16 * cc);
+        a = dot2_bf16(x.x, y.x, a);
+        b = dot2_bf16(x.y, y.y, b);
+        a = dot2_bf16(x.z, y.z, a);
+        b = dot2_bf16(x.w, y.w, b);
+    }
+    return a + b;
+}
+
+__device__ __forceinline__ float row_dot_global_shared(const float *o, const uint8_t *g, int lane) {
+    const float4 *o4 = reinterpret_cast<const float4 *>(o);
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const int cc = (c + lane) & 15;
+        const float4 x = __ldg(o4 + cc);
+        const float4 y = *reinterpret_cast<const float4 *>(g + 16 * cc);
+        a = fmaf(x.x, y.x, a);
+        b = fmaf(x.y, y.y, b);
+        a = fmaf(x.z, y.z, a);
+        b = fmaf(x.w, y.w, b);
+    }
+    return a + b;
+}
 
 struct BwdParams {
     const void *Q, *K, *V, *O, *dO;
@@ -441,7 +477,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     constexpr int RB = S::kRowBytes;
     constexpr int R = 32 / G;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ uint64_t full_bar[2], empty_bar[2];
+    __shared__ uint64_t full_bar[2], empty_bar[2], aux_bar[2];
     __shared__ int s_off[kMaxEntries];
 
     const int N = tab.N;
@@ -451,32 +487,48 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
+            mbar_init(&aux_bar[s], 1);
         }
     }
     __syncthreads();
-    grid_dep_launch();
     grid_dep_wait();
-    const size_t tens = (size_t)N * RB;   // one tensor's rows in a stage: Q | K | V | dO
+    grid_dep_launch();
+    const size_t tens = (size_t)N * RB;   // one tensor's rows in a stage: Q | K | V | dO | D | LSE2
     if (warp == 0) {
-        if (lane != 0) return;
+        // producer warp: lane 0 streams the unit's four tensors in; then the
+        // whole warp fills the stage's per-row terms D_j = <dO_j, O_j> (O read
+        // from global memory, prefetched into L2 a unit ahead) and LSE_j in
+        // log2 units, so no consumer waits on a global load
         int i = 0;
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
             const int s = i % p.stages;
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)u * N;
-            const uint32_t b = (uint32_t)tens;
-            mbar_expect_tx(&full_bar[s], 4 * b);
-            bulk_g2s(st, static_cast<const T *>(p.Q) + row0 * kHeadDim, b, &full_bar[s]);
-            bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
-            bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
-            bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
-            const int un = u + gridDim.x;
-            if (un < p.n_units) {
-                bulk_prefetch_l2(static_cast<const T *>(p.O) + (size_t)un * N * kHeadDim, b);
-                if ((N * 4) % 16 == 0 && ((size_t)un * N * 4) % 16 == 0)
-                    bulk_prefetch_l2(p.LSE + (size_t)un * N, (uint32_t)N * 4);
+            if (lane == 0) {
+                const uint32_t b = (uint32_t)tens;
+                mbar_expect_tx(&full_bar[s], 4 * b);
+                bulk_g2s(st, static_cast<const T *>(p.Q) + row0 * kHeadDim, b, &full_bar[s]);
+                bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
+                bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
+                bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
+                const int un = u + gridDim.x;
+                if (un < p.n_units) {
+                    bulk_prefetch_l2(static_cast<const T *>(p.O) + (size_t)un * N * kHeadDim, b);
+                    if ((N * 4) % 16 == 0 && ((size_t)un * N * 4) % 16 == 0)
+                        bulk_prefetch_l2(p.LSE + (size_t)un * N, (uint32_t)N * 4);
+                }
             }
+            __syncwarp();
+            if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
+            float *sD = reinterpret_cast<float *>(st + 4 * tens), *sL = sD + N;
+            for (int j = lane; j < N; j += 32) {
+                sD[j] = row_dot_global_shared(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim,
+                                              st + 3 * tens + (size_t)j * RB, lane);
+                sL[j] = p.LSE[row0 + j] * kLog2e;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aux_bar[s]);
         }
         return;
     }
@@ -491,8 +543,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
         const int s = i % p.stages;
         if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
+        if (!mbar_wait(&aux_bar[s], (i / p.stages) & 1)) return;
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         const uint8_t *sQ = st, *sK = st + tens;
+        const float *sD = reinterpret_cast<const float *>(st + 4 * tens), *sL = sD + N;
         const int h = u % tab.H;
         const int t0 = tab.start[h], t1 = tab.start[h + 1];
         const size_t row0 = (size_t)u * N;
@@ -504,12 +558,11 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             const int jfirst = r * R, jlast = min(N, r * R + R) - 1;
             int tb = t0, te = t0;
             if (t1 > t0) round_range(s_off, N, t0, t1, jfirst, jlast, tb, te);
-            S q, g, o;
+            S q, g;
             q.load(sQ + (size_t)j * RB, lg.c);
             g.load(sQ + 3 * tens + (size_t)j * RB, lg.c);
-            o.load_global(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim, lg.c);
-            const float Dj = group_sum<G>(g.dot(o));
-            const float lse2 = p.LSE[row0 + j] * kLog2e;
+            const float Dj = sD[j];
+            const float lse2 = sL[j];
             float2 dq[32 / G];
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
@@ -553,27 +606,20 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 // pair weights P and dS in a global scratch [b, h][2][max_count][N] (phase A
 // writes the pairs in range, phase B reads exactly those).  Phase A: dQ;
 // phase B: dK, dV.  Block: kFlatWarps warps of one (b, h), one round each.
-template <typename T, int G, int W = kFlatWarps>
-__global__ void __launch_bounds__(W * 32)
-bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float *scr) {
+template <typename T, int G>
+__device__ __forceinline__ void bwd_flat_a_round(const TableArg &tab, const BwdParams &p, const int *s_off,
+                                                 float *scr, int bh, int r) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
     constexpr int R = 32 / G;
-    __shared__ int s_off[kMaxEntries];
     const int N = tab.N;
-    const int bh = blockIdx.x, h = bh % tab.H;
+    const int h = bh % tab.H;
     const int t0 = tab.start[h], t1 = tab.start[h + 1];
-    for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
-    __syncthreads();
-    grid_dep_launch();
-    grid_dep_wait();
     const int lane = threadIdx.x & 31;
-    const int r = blockIdx.y * W + (threadIdx.x >> 5);
-    if (r * R >= N) return;
     const size_t row0 = (size_t)bh * N;
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB;
     const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
-    float *scrP = scr + (size_t)bh * 2 * p.max_count * N;
+    float *scrP = scr;   // this unit's weights
     float *scrS = scrP + (size_t)p.max_count * N;
     const LaneGeom<T, G> lg;
     const int jl = r * R + lane / G;
@@ -602,25 +648,43 @@ bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float
 
 template <typename T, int G, int W = kFlatWarps>
 __global__ void __launch_bounds__(W * 32)
-bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const float *scr) {
+bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float *scr, int bh0) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
     constexpr int R = 32 / G;
     __shared__ int s_off[kMaxEntries];
     const int N = tab.N;
-    const int bh = blockIdx.x, h = bh % tab.H;
+    const int bh = bh0 + blockIdx.x, h = bh % tab.H;
     const int t0 = tab.start[h], t1 = tab.start[h + 1];
     for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
     __syncthreads();
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
+    const int r = blockIdx.y * W + (threadIdx.x >> 5);
+    if (r * R < N) bwd_flat_a_round<T, G>(tab, p, s_off, scr + (size_t)blockIdx.x * 2 * p.max_count * N, bh, r);
+}
+
+template <typename T, int G, int W = kFlatWarps>
+__global__ void __launch_bounds__(W * 32)
+bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const float *scr, int bh0) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
+    __shared__ int s_off[kMaxEntries];
+    const int N = tab.N;
+    const int bh = bh0 + blockIdx.x, h = bh % tab.H;
+    const int t0 = tab.start[h], t1 = tab.start[h + 1];
+    for (int t = t0 + (int)threadIdx.x; t < t1; t += blockDim.x) s_off[t] = tab.off[t];
+    __syncthreads();
+    grid_dep_wait();
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.y * W + (threadIdx.x >> 5);
     if (r * R >= N) return;
     const size_t row0 = (size_t)bh * N;
     const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB;
     const ptrdiff_t gdelta = static_cast<const uint8_t *>(p.dO) - static_cast<const uint8_t *>(p.Q);
-    const float *scrP = scr + (size_t)bh * 2 * p.max_count * N;
+    const float *scrP = scr + (size_t)blockIdx.x * 2 * p.max_count * N;   // this unit's weights
     const float *scrS = scrP + (size_t)p.max_count * N;
     const LaneGeom<T, G> lg;
     const int kl = r * R + lane / G;
@@ -799,7 +863,7 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     if (const char *e = getenv("FIBATT_BWD_THREADS")) maxt = atoi(e) == 1024 ? 1024 : 512;
     if (G == 2) maxt = 512;
     const int maxw = maxt / 32;
-    const size_t stage = (4 * (size_t)N * RB + 127) / 128 * 128;
+    const size_t stage = (4 * (size_t)N * RB + 2 * (size_t)N * sizeof(float) + 127) / 128 * 128;
     const size_t scratch = (2 * (size_t)std::max(1, tab.max_count) * N * 4 + 127) / 128 * 128;
     int stages = stage * 2 + scratch <= budget ? 2 : (stage + scratch <= budget ? 1 : 0);
     if (const char *e = getenv("FIBATT_STAGES")) stages = std::min(stages, std::max(1, atoi(e)));
@@ -823,7 +887,7 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
 }
 
 template <typename T>
-static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
+static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int units) {
     int dev = 0;
     cudaGetDevice(&dev);
     const int ti = std::is_same<T, float>::value ? 0 : 1;
@@ -836,7 +900,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
         g_bwd_smem_set[ki][dev] = pl.smem;
     }
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                a.B * a.tab->H, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
+                units, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
                 (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count)};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
@@ -844,19 +908,22 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Units [bh0, bh0 + count); the scratch a.Dws holds `count` units' weights.
 template <typename T, int G, int W = kFlatWarps>
-static cudaError_t bwd_flat(const BwdArgs &a) {
+static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count)};
-    const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * W - 1) / (R * W)));
+    const dim3 grid((unsigned)count, (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
-    cudaError_t e = launch_kernel(bwd_flat_a_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p, a.Dws);
+    float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N
+    cudaError_t e =
+        launch_kernel(bwd_flat_a_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p, scr, bh0);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_kernel(bwd_flat_b_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p,
-                      static_cast<const float *>(a.Dws));
+                      static_cast<const float *>(scr), bh0);
     count_launches(2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -864,8 +931,9 @@ static cudaError_t bwd_flat(const BwdArgs &a) {
 cudaError_t launch_bwd_flat(const BwdArgs &a) {
     int G = 4;
     if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
-    if (a.dtype == FIBATT_F32) return bwd_flat<float, 4>(a);
-    return G == 2 ? bwd_flat<__nv_bfloat16, 2>(a) : bwd_flat<__nv_bfloat16, 4>(a);
+    const int units = a.B * a.tab->H;
+    if (a.dtype == FIBATT_F32) return bwd_flat<float, 4>(a, 0, units);
+    return G == 2 ? bwd_flat<__nv_bfloat16, 2>(a, 0, units) : bwd_flat<__nv_bfloat16, 4>(a, 0, units);
 }
 
 size_t flat_bwd_scratch_bytes(const TableArg &tab, int B) {
@@ -873,7 +941,8 @@ size_t flat_bwd_scratch_bytes(const TableArg &tab, int B) {
 }
 
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
-    return a.dtype == FIBATT_F32 ? bwd_resident<float>(a, pl) : bwd_resident<__nv_bfloat16>(a, pl);
+    const int units = a.B * a.tab->H;
+    return a.dtype == FIBATT_F32 ? bwd_resident<float>(a, pl, units) : bwd_resident<__nv_bfloat16>(a, pl, units);
 }
 
 template <typename T, int G, int W = kFlatWarps, int U = 2>
