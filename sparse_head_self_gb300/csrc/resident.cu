@@ -24,8 +24,12 @@
 //         so the rescale is rare and p = 2^(s - m) <= 2^8 never overflows;
 //   acc += p * v_{j+d} with packed f32x2 fmas;
 //   O = acc / l (RNE to the I/O dtype), LSE = ln 2 * (m + log2 l).
-// Offsets that reach a key for every row of a warp's 16 rows run without
-// range predicates; only the edge offsets of a round are predicated.
+// Edges are branch-free: per round, two warp ballots drop the offsets that
+// reach no key for any row of the round; the rest read a clamped row and
+// mask the score of an out-of-range key to -inf.
+//
+// The flat kernels further down run the same round code on rows read from
+// global memory, for heads whose key windows do not fit in shared memory.
 #include <algorithm>
 #include <cstdlib>
 #include <type_traits>
