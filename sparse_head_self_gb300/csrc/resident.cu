@@ -56,6 +56,13 @@ struct PipeParams {
     int gwarps;        // warps per consumer group
     uint32_t stage_bytes;
     int prefetch;      // units beyond the ring warmed in L2
+    // The last wave: units [n_keep, n_keep + (qsplit units left) * qsub) are
+    // the regular units n_keep, n_keep + 1, ... cut into qsub sub-units of
+    // sub_rows query rows, so the wave that does not fill every CTA is
+    // spread thin instead of landing whole on a few CTAs.
+    int n_keep;
+    int qsub;
+    int sub_rows;
 };
 
 struct Unit {
@@ -64,10 +71,18 @@ struct Unit {
 
 __device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const PipeParams &p, int u) {
     Unit g;
-    g.bh = u / p.qsplit;
+    if (u < p.n_keep) {
+        g.bh = u / p.qsplit;
+        g.q0 = (u % p.qsplit) * p.chunk;
+        g.q1 = min(tab.N, g.q0 + p.chunk);
+    } else {
+        const int s = u - p.n_keep, ur = p.n_keep + s / p.qsub;
+        g.bh = ur / p.qsplit;
+        const int cb = (ur % p.qsplit) * p.chunk, ce = min(tab.N, cb + p.chunk);
+        g.q0 = min(ce, cb + (s % p.qsub) * p.sub_rows);
+        g.q1 = min(ce, g.q0 + p.sub_rows);
+    }
     g.h = g.bh % tab.H;
-    g.q0 = (u % p.qsplit) * p.chunk;
-    g.q1 = min(tab.N, g.q0 + p.chunk);
     g.t0 = tab.start[g.h];
     g.t1 = tab.start[g.h + 1];
     g.lo = 0;
@@ -226,7 +241,8 @@ __device__ __forceinline__ void prefetch_unit(const TableArg &tab, const PipePar
     constexpr int RB = sizeof(T) * kHeadDim;
     const Unit g = unit_geometry(tab, p, u);
     const size_t row0 = (size_t)g.bh * tab.N;
-    bulk_prefetch_l2(static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, (uint32_t)(g.q1 - g.q0) * RB);
+    if (g.q1 > g.q0)
+        bulk_prefetch_l2(static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, (uint32_t)(g.q1 - g.q0) * RB);
     if (g.nrows) {
         bulk_prefetch_l2(static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, (uint32_t)g.nrows * RB);
         bulk_prefetch_l2(static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, (uint32_t)g.nrows * RB);
@@ -277,7 +293,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
             const size_t row0 = (size_t)g.bh * tab.N;
             const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
             mbar_expect_tx(&full_bar[s], qb + 2 * kvb);
-            bulk_g2s(st + q_off, static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, qb, &full_bar[s]);
+            if (qb)   // a last-wave piece past the end of its chunk has no rows
+                bulk_g2s(st + q_off, static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, qb, &full_bar[s]);
             if (kvb) {
                 bulk_g2s(st + k_off, static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
                 bulk_g2s(st + v_off, static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
@@ -816,6 +833,21 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->threads = 32 * (1 + groups * gwarps);
     const long units = (long)B * tab.H * qsplit;
     pl->grid = (int)std::min<long>(units, sms);
+    // cut the units of the last, partial wave into single rounds (at most as
+    // many pieces as there are CTAs)
+    pl->n_keep = (int)units;
+    pl->qsub = 1;
+    pl->sub_rows = chunk;
+    const long left = units > pl->grid ? units % pl->grid : 0;
+    const char *st = getenv("FIBATT_SPLIT_TAIL");
+    if (left > 0 && !(st && atoi(st) == 0)) {
+        const int qsub = (int)std::max<long>(1, std::min<long>(chunk / R, pl->grid / left));
+        if (qsub > 1) {
+            pl->n_keep = (int)(units - left);
+            pl->qsub = qsub;
+            pl->sub_rows = ((chunk + qsub - 1) / qsub + R - 1) / R * R;
+        }
+    }
     return true;
 }
 
@@ -831,9 +863,10 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
         if (e != cudaSuccess) return e;
         g_fwd_smem_set[ti][dev] = pl.smem;
     }
+    const int n_reg = a.B * a.tab->H * pl.qsplit;
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
-                 a.B * a.tab->H * pl.qsplit, pl.stages, pl.groups, pl.gwarps, (uint32_t)pl.stage_bytes,
-                 pl.prefetch};
+                 pl.n_keep + (n_reg - pl.n_keep) * pl.qsub, pl.stages, pl.groups, pl.gwarps,
+                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -877,6 +910,9 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->unroll = 1;
     pl->maxt = maxt;
     pl->prefetch = 0;
+    pl->n_keep = 0;
+    pl->qsub = 1;
+    pl->sub_rows = N;
     pl->qsplit = 1;
     pl->chunk = N;
     pl->kv_cap = N;

@@ -121,6 +121,18 @@ def test_resident_query_chunks(qsplit, dtype, monkeypatch):
     _fwd_full(wl, seed=23)
 
 
+@pytest.mark.parametrize("split", ["0", "1"])
+def test_resident_last_wave_pieces(split, monkeypatch):
+    # 7 x 12 heads x 2 chunks = 168 units on (at most) 152 CTAs: the units of
+    # the partial last wave are cut into one-round pieces, some of them past
+    # the end of their chunk (empty)
+    monkeypatch.setenv("FIBATT_PATH", "resident")
+    monkeypatch.setenv("FIBATT_QSPLIT", "2")
+    monkeypatch.setenv("FIBATT_SPLIT_TAIL", split)
+    wl = WORKLOADS["vitb"].with_batch(7)
+    _fwd_full(wl, seed=13)
+
+
 @pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 def test_empty_support_rows_are_zero(kernel_path):
     # N = 3, row 2 of the Wythoff array (4, 7), no diagonal: no pair at all
