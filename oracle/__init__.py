@@ -158,28 +158,31 @@ def windows(h: int, w_min: int, w_max: int) -> list[int]:
 # ------------------------------------------------------------------- support
 
 class Head:
-    """One head's support: distance set S, window w, diagonal flag."""
+    """One head's support: distance set S, window w, diagonal flag, and the
+    optional global first token (README Algorithm 2: row 0 and column 0 of
+    the mask are all ones)."""
 
-    def __init__(self, S, w: int, diag: bool):
+    def __init__(self, S, w: int, diag: bool, global_token: bool = False):
         self.S = np.ascontiguousarray(np.asarray(list(S), dtype=np.int64))
         self.w = int(w)
         self.diag = 1 if diag else 0
+        self.global_token = bool(global_token)
 
     @classmethod
-    def fibottention(cls, a: int, b: int, w: int, diag: bool) -> "Head":
-        return cls(fib_list(a, b, w), w, diag)
+    def fibottention(cls, a: int, b: int, w: int, diag: bool, global_token: bool = False) -> "Head":
+        return cls(fib_list(a, b, w), w, diag, global_token)
 
     def _args(self):
-        return _ptr(self.S, _i64p), int(self.S.size), self.w, self.diag
+        return _ptr(self.S, _i64p), int(self.S.size), self.w, self.diag | (2 if self.global_token else 0)
 
 
 def wythoff_heads(H: int, N: int, w_min: int, w_max: int, diag: bool,
-                  first_row: int = 1) -> list[Head]:
+                  first_row: int = 1, global_token: bool = False) -> list[Head]:
     """Heads 1..H on Wythoff rows first_row.. with the linear window schedule."""
     heads = []
     for i in range(1, H + 1):
         a, b = wythoff_row(first_row + i - 1)
-        heads.append(Head.fibottention(a, b, window(i, H, w_min, w_max), diag))
+        heads.append(Head.fibottention(a, b, window(i, H, w_min, w_max), diag, global_token))
     return heads
 
 

@@ -32,6 +32,11 @@
  *   - The backward pass is the exact derivative of the forward pass with
  *     respect to Q, K and V for the loss L = sum(dO * O); the pages print no
  *     backward, so it is derived here from the softmax Jacobian.
+ *   - Global first token ([P2] Algorithm 2 leaves row 0 and column 0 of its
+ *     mask all ones: the class token attends every key and every query
+ *     attends it).  Optional, selected by bit 1 of the flags argument (bit 0
+ *     is the diagonal): (j,k) with j == 0 or k == 0 is then in Omega too.
+ *     The signed-offset table describes the banded part only.
  *
  * Every loop below visits (j,k) pairs by brute force over the whole N x N
  * index square and tests membership from the definition; nothing is tiled,
@@ -136,11 +141,13 @@ int64_t orc_window(int64_t i, int64_t h, int64_t w_min, int64_t w_max)
 /* ----------------------------------------------------------------- support */
 
 /* [P1] Sec. 3: (j,k) is in Omega_w^{S} iff |j-k| is one of the distances in S
- * and |j-k| <= w; the main diagonal is added when diag is set. */
-int orc_in_support(int64_t j, int64_t k, const int64_t *S, int nS, int64_t w, int diag)
+ * and |j-k| <= w; the main diagonal is added when bit 0 of flags is set, and
+ * row 0 and column 0 ([P2] Algorithm 2) when bit 1 is set. */
+int orc_in_support(int64_t j, int64_t k, const int64_t *S, int nS, int64_t w, int flags)
 {
     int64_t d = j > k ? j - k : k - j;
-    if (diag && d == 0) return 1;
+    if ((flags & 2) && (j == 0 || k == 0)) return 1;
+    if ((flags & 1) && d == 0) return 1;
     if (d > w) return 0;
     for (int t = 0; t < nS; ++t)
         if (S[t] == d) return 1;
@@ -148,12 +155,12 @@ int orc_in_support(int64_t j, int64_t k, const int64_t *S, int nS, int64_t w, in
 }
 
 /* Dense N x N 0/1 mask of Omega, by testing every pair.  Returns |Omega|. */
-int64_t orc_support_mask(int64_t N, const int64_t *S, int nS, int64_t w, int diag, uint8_t *mask)
+int64_t orc_support_mask(int64_t N, const int64_t *S, int nS, int64_t w, int flags, uint8_t *mask)
 {
     int64_t count = 0;
     for (int64_t j = 0; j < N; ++j)
         for (int64_t k = 0; k < N; ++k) {
-            int in = orc_in_support(j, k, S, nS, w, diag);
+            int in = orc_in_support(j, k, S, nS, w, flags);
             if (mask) mask[j * N + k] = (uint8_t)in;
             count += in;
         }
@@ -163,8 +170,9 @@ int64_t orc_support_mask(int64_t N, const int64_t *S, int nS, int64_t w, int dia
 /* Signed offsets delta = k - j present in Omega, ascending, read off the
  * first row (j = 0, delta = k >= 0) and first column (k = 0, delta = -j <= 0)
  * of Omega.  Writes at most cap entries, returns the number present. */
-int orc_signed_table(int64_t N, const int64_t *S, int nS, int64_t w, int diag, int32_t *out, int cap)
+int orc_signed_table(int64_t N, const int64_t *S, int nS, int64_t w, int flags, int32_t *out, int cap)
 {
+    const int diag = flags & 1;   /* the banded part: no global first token */
     int n = 0;
     for (int64_t j = N - 1; j >= 1; --j)            /* column 0: delta = -j */
         if (orc_in_support(j, 0, S, nS, w, diag)) {
@@ -187,13 +195,13 @@ int orc_signed_table(int64_t N, const int64_t *S, int nS, int64_t w, int diag, i
  * leaves every quotient unchanged.  Fills kidx/p with the support of the row,
  * returns its size and writes log(sum_l e^{s_l}) to *lse (-inf if empty). */
 static int64_t row_softmax(int64_t N, int64_t Dh, const double *Q, const double *K,
-                           const int64_t *S, int nS, int64_t w, int diag, double scale,
+                           const int64_t *S, int nS, int64_t w, int flags, double scale,
                            int64_t j, int64_t *kidx, double *p, double *lse)
 {
     int64_t n = 0;
     double m = -INFINITY;
     for (int64_t k = 0; k < N; ++k) {
-        if (!orc_in_support(j, k, S, nS, w, diag)) continue;
+        if (!orc_in_support(j, k, S, nS, w, flags)) continue;
         double s = 0.0;
         for (int64_t d = 0; d < Dh; ++d) s += Q[j * Dh + d] * K[k * Dh + d];
         s *= scale;
@@ -218,7 +226,7 @@ static int64_t row_softmax(int64_t N, int64_t Dh, const double *Q, const double 
  * row-major; O is nrows x Dh and LSE has nrows entries, in the order of
  * rows. */
 void orc_fwd_rows(int64_t N, int64_t Dh, const double *Q, const double *K, const double *V,
-                  const int64_t *S, int nS, int64_t w, int diag, double scale,
+                  const int64_t *S, int nS, int64_t w, int flags, double scale,
                   const int64_t *rows, int64_t nrows, double *O, double *LSE)
 {
     if (!rows) nrows = N;
@@ -230,7 +238,7 @@ void orc_fwd_rows(int64_t N, int64_t Dh, const double *Q, const double *K, const
         for (int64_t r = 0; r < nrows; ++r) {
             int64_t j = rows ? rows[r] : r;
             double lse;
-            int64_t n = row_softmax(N, Dh, Q, K, S, nS, w, diag, scale, j, kidx, p, &lse);
+            int64_t n = row_softmax(N, Dh, Q, K, S, nS, w, flags, scale, j, kidx, p, &lse);
             LSE[r] = lse;
             for (int64_t d = 0; d < Dh; ++d) {
                 double o = 0.0;
@@ -249,11 +257,11 @@ void orc_fwd_rows(int64_t N, int64_t Dh, const double *Q, const double *K, const
  * dP_jk = <dO_j, V_k>, D_j = sum_l P_jl dP_jl, dS_jk = P_jk (dP_jk - D_j).
  * Fills kidx, p and ds with the row's support; returns its size. */
 static int64_t row_ds(int64_t N, int64_t Dh, const double *Q, const double *K, const double *V,
-                      const double *dO, const int64_t *S, int nS, int64_t w, int diag,
+                      const double *dO, const int64_t *S, int nS, int64_t w, int flags,
                       double scale, int64_t j, int64_t *kidx, double *p, double *ds)
 {
     double lse;
-    int64_t n = row_softmax(N, Dh, Q, K, S, nS, w, diag, scale, j, kidx, p, &lse);
+    int64_t n = row_softmax(N, Dh, Q, K, S, nS, w, flags, scale, j, kidx, p, &lse);
     double Dj = 0.0;
     for (int64_t t = 0; t < n; ++t) {
         double dp = 0.0;
@@ -274,7 +282,7 @@ static int64_t row_ds(int64_t N, int64_t Dh, const double *Q, const double *K, c
  * krows (all rows when the list is NULL); outputs are packed in list order.
  * Pass dQ = NULL or dK = dV = NULL to skip that part. */
 void orc_bwd_rows(int64_t N, int64_t Dh, const double *Q, const double *K, const double *V,
-                  const double *dO, const int64_t *S, int nS, int64_t w, int diag, double scale,
+                  const double *dO, const int64_t *S, int nS, int64_t w, int flags, double scale,
                   const int64_t *qrows, int64_t nq, const int64_t *krows, int64_t nk,
                   double *dQ, double *dK, double *dV)
 {
@@ -290,7 +298,7 @@ void orc_bwd_rows(int64_t N, int64_t Dh, const double *Q, const double *K, const
 #pragma omp for schedule(dynamic, 4)
             for (int64_t r = 0; r < nq; ++r) {
                 int64_t j = qrows ? qrows[r] : r;
-                int64_t n = row_ds(N, Dh, Q, K, V, dO, S, nS, w, diag, scale, j, kidx, p, ds);
+                int64_t n = row_ds(N, Dh, Q, K, V, dO, S, nS, w, flags, scale, j, kidx, p, ds);
                 for (int64_t d = 0; d < Dh; ++d) {
                     double g = 0.0;
                     for (int64_t t = 0; t < n; ++t) g += ds[t] * K[kidx[t] * Dh + d];
@@ -308,8 +316,8 @@ void orc_bwd_rows(int64_t N, int64_t Dh, const double *Q, const double *K, const
                 }
                 /* every query row j whose support contains key k */
                 for (int64_t j = 0; j < N; ++j) {
-                    if (!orc_in_support(j, k, S, nS, w, diag)) continue;
-                    int64_t n = row_ds(N, Dh, Q, K, V, dO, S, nS, w, diag, scale, j, kidx, p, ds);
+                    if (!orc_in_support(j, k, S, nS, w, flags)) continue;
+                    int64_t n = row_ds(N, Dh, Q, K, V, dO, S, nS, w, flags, scale, j, kidx, p, ds);
                     for (int64_t t = 0; t < n; ++t) {
                         if (kidx[t] != k) continue;
                         for (int64_t d = 0; d < Dh; ++d) {

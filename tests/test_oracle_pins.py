@@ -330,3 +330,88 @@ def test_bwd_gradient_sums():
     head = oracle.Head.fibottention(1, 2, 8, True)
     _, dK, _ = oracle.bwd_head(Q, K, V, dO, head, 0.4)
     np.testing.assert_allclose(dK.sum(axis=0), 0.0, atol=1e-12)
+
+
+# ------------------------------------------------- global first token (CLS)
+#
+# README Algorithm 2 leaves row 0 and column 0 of its (N+1) x (N+1) mask all
+# ones: the class token attends every key and every token attends it.
+
+def _global_mask_by_definition(N, S, w, diag):
+    """Omega by the set definition, plus row 0 and column 0 (numpy only)."""
+    j = np.arange(N)[:, None]
+    k = np.arange(N)[None, :]
+    d = np.abs(j - k)
+    M = np.isin(d, np.asarray(list(S), dtype=np.int64)) & (d <= w)
+    if diag:
+        M |= d == 0
+    M[0, :] = True
+    M[:, 0] = True
+    return M
+
+
+@pytest.mark.parametrize("N,S,w,diag", [(1, [1, 2], 5, False), (2, [], 2, False), (9, [1, 2, 3, 5, 8], 5, True),
+                                        (40, [4, 7, 11, 18, 29], 30, False), (65, [6, 10, 16, 26, 42], 65, True)])
+def test_global_token_support(N, S, w, diag):
+    head = oracle.Head(S, w, diag, global_token=True)
+    M = oracle.support_mask(N, head)
+    assert np.array_equal(M.astype(bool), _global_mask_by_definition(N, S, w, diag))
+    # closed form: the banded pairs, plus the 2N - 1 pairs of row/column 0,
+    # minus those of row/column 0 that are banded already (c on each, the
+    # diagonal pair (0, 0) counted once)
+    c = sum(1 for f in set(S) if 1 <= f <= min(w, N - 1)) + (1 if diag or 0 in S else 0)
+    base = oracle.support_size(N, oracle.Head(S, w, diag))
+    assert oracle.support_size(N, head) == base + (2 * N - 1) - (2 * c - (1 if diag or 0 in S else 0))
+    # the signed table describes the banded part only
+    assert np.array_equal(oracle.signed_table(N, head), oracle.signed_table(N, oracle.Head(S, w, diag)))
+
+
+def test_global_token_only_support():
+    # no distances, no diagonal: query 0 is plain softmax attention over every
+    # key, and every other query attends key 0 alone (its output is V_0)
+    N, Dh, scale = 17, 8, 0.3
+    Q, K, V = _rand((N, Dh), 60), _rand((N, Dh), 61), _rand((N, Dh), 62)
+    head = oracle.Head([], N, False, global_token=True)
+    O, L = oracle.fwd_head(Q, K, V, head, scale)
+    O_ref, L_ref = _dense_ref(Q[:1], K, V, scale)
+    np.testing.assert_allclose(O[0], O_ref[0], atol=1e-12, rtol=0)
+    np.testing.assert_allclose(L[0], L_ref[0], atol=1e-12, rtol=0)
+    assert np.array_equal(O[1:], np.broadcast_to(V[0], (N - 1, Dh)))
+    np.testing.assert_allclose(L[1:], scale * Q[1:] @ K[0], atol=1e-13, rtol=0)
+
+
+def test_global_token_fwd_bwd_match_torch_masked_dense():
+    N, Dh, scale = 33, 16, 0.125
+    Q, K, V, dO = (_rand((N, Dh), 70 + s) for s in range(4))
+    for head in oracle.wythoff_heads(3, N, 5, 33, True, global_token=True) + \
+            oracle.wythoff_heads(2, N, 4, 20, False, global_token=True):
+        M = torch.from_numpy(_global_mask_by_definition(N, head.S, head.w, bool(head.diag)))
+        q, k, v = (torch.tensor(x, requires_grad=True) for x in (Q, K, V))
+        s = (scale * q @ k.T).masked_fill(~M, float("-inf"))
+        o = torch.softmax(s, dim=1) @ v
+        o.backward(torch.from_numpy(dO))
+        O, L = oracle.fwd_head(Q, K, V, head, scale)
+        np.testing.assert_allclose(O, o.detach().numpy(), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(L, torch.logsumexp(s, dim=1).detach().numpy(), atol=1e-12, rtol=0)
+        dQ, dK, dV = oracle.bwd_head(Q, K, V, dO, head, scale)
+        np.testing.assert_allclose(dQ, q.grad.numpy(), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(dK, k.grad.numpy(), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(dV, v.grad.numpy(), atol=1e-12, rtol=0)
+
+
+def test_global_token_bwd_central_finite_differences():
+    N, Dh, scale, h = 11, 4, 0.5, 1e-6
+    Q, K, V, dO = (_rand((N, Dh), 80 + s) for s in range(4))
+    head = oracle.Head.fibottention(4, 7, 9, False, global_token=True)
+    dQ, dK, dV = oracle.bwd_head(Q, K, V, dO, head, scale)
+    for X, G in [(Q, dQ), (K, dK), (V, dV)]:
+        num = np.zeros_like(X)
+        for idx in np.ndindex(*X.shape):
+            old = X[idx]
+            X[idx] = old + h
+            lp = _loss(Q, K, V, dO, head, scale)
+            X[idx] = old - h
+            lm = _loss(Q, K, V, dO, head, scale)
+            X[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(G, num, atol=2e-7, rtol=0)
