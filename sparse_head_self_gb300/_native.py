@@ -35,6 +35,7 @@ _SIGS = {
                                             ctypes.c_int, ctypes.POINTER(_vp)]),
     "fibatt_support_build_distances": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _i32p, _i32p,
                                                       ctypes.c_int, ctypes.POINTER(_vp)]),
+    "fibatt_support_set_global_token": (ctypes.c_int, [_vp, ctypes.c_int]),
     "fibatt_support_info": (ctypes.c_int, [_vp, _ip, _ip, _ip]),
     "fibatt_support_get": (ctypes.c_int, [_vp, _i32p, _i32p, _i64p]),
     "fibatt_support_destroy": (None, [_vp]),

@@ -94,6 +94,12 @@ class Support:
         return cls.build(N, [ab[p][0] for p in perm], [ab[p][1] for p in perm], [w[p] for p in perm],
                          include_diag)
 
+    def set_global_token(self, enabled: bool = True) -> "Support":
+        """fibatt_support_set_global_token: token 0 attends every key and is
+        attended by every query (README Algorithm 2's class token)."""
+        check(lib().fibatt_support_set_global_token(self._h, int(bool(enabled))))
+        return self
+
     # -- queries -------------------------------------------------------------
     def tables(self):
         """(counts[H], signed offsets (CSR), pairs[H])."""

@@ -81,6 +81,7 @@ fibatt_status finish_support(int H, int N, const std::vector<std::set<int64_t>> 
     tab.H = H;
     tab.N = N;
     s->impl.pairs.assign(H, 0);
+    s->impl.global_pairs.assign(H, 0);
     int n = 0;
     for (int h = 0; h < H; ++h) {
         tab.start[h] = n;
@@ -101,6 +102,11 @@ fibatt_status finish_support(int H, int N, const std::vector<std::set<int64_t>> 
         for (int64_t f : d)
             if (f > 0) pairs += 2 * (int64_t)(N - f);
         s->impl.pairs[h] = pairs;
+        // row 0 and column 0 hold 2N - 1 pairs; the banded ones among them
+        // are (0, f) and (f, 0) for every distance f, and (0, 0) once
+        int64_t npos = 0;
+        for (int64_t f : d) npos += f > 0;
+        s->impl.global_pairs[h] = 2 * (int64_t)N - 1 - 2 * npos - (zero ? 1 : 0);
         for (int32_t o : row) {
             tab.off[n++] = o;
             tab.max_abs = std::max(tab.max_abs, o < 0 ? -o : o);
@@ -331,9 +337,16 @@ fibatt_status fibatt_support_get(fibatt_support_t s, int32_t *counts, int32_t *s
     const TableArg &tab = s->impl.tab;
     for (int h = 0; h < tab.H; ++h) {
         if (counts) counts[h] = tab.start[h + 1] - tab.start[h];
-        if (pairs) pairs[h] = s->impl.pairs[h];
+        if (pairs) pairs[h] = s->impl.pairs[h] + (tab.global0 ? s->impl.global_pairs[h] : 0);
     }
     if (signed_offsets) std::memcpy(signed_offsets, tab.off, sizeof(int32_t) * tab.start[tab.H]);
+    return FIBATT_OK;
+}
+
+fibatt_status fibatt_support_set_global_token(fibatt_support_t s, int enabled) {
+    if (!s) return set_error(FIBATT_ERR_INVALID_ARG, "support handle is NULL");
+    forget_plans(s);   // stage sizes depend on it
+    s->impl.tab.global0 = enabled ? 1 : 0;
     return FIBATT_OK;
 }
 
@@ -355,6 +368,8 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     const PathSel sel = path_sel();
     ResidentPlan pl;
     cudaError_t e;
+    if (s->impl.tab.global0 && sel == PathSel::Generic)
+        return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=generic has no global first token");
     if (sel == PathSel::Generic) {
         e = launch_fwd_generic(a);
     } else if (sel != PathSel::Flat && cached_plan(s, false, s->impl.tab, B, dtype, &pl)) {
@@ -364,15 +379,23 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
             return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: windows do not fit in shared memory");
         e = launch_fwd_flat(a);
     }
+    if (e == cudaSuccess && s->impl.tab.global0) e = launch_fwd_global_row(a);
     if (e != cudaSuccess) return cuda_error(e, "fibatt_fwd launch");
     return FIBATT_OK;
+}
+
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// P_0k and dS_0k of every key of every (b, h) when token 0 is global.
+static size_t global_ws_bytes(const TableArg &tab, int B) {
+    return tab.global0 ? (size_t)B * tab.H * 2 * tab.N * sizeof(float) : 0;
 }
 
 size_t fibatt_bwd_workspace_bytes(fibatt_support_t s, int B) {
     if (!s || B < 1) return 0;
     const size_t rows = (size_t)B * s->impl.tab.H * s->impl.tab.N;
     const size_t bytes = std::max(rows * sizeof(float), flat_bwd_scratch_bytes(s->impl.tab, B));
-    return (bytes + 255) / 256 * 256;
+    return round256(bytes) + round256(global_ws_bytes(s->impl.tab, B));
 }
 
 enum class BwdPath { Resident, Flat, Generic };
@@ -382,16 +405,17 @@ enum class BwdPath { Resident, Flat, Generic };
 static size_t bwd_workspace_needed(fibatt_support_t s, int B, fibatt_dtype dt, BwdPath *path, ResidentPlan *pl) {
     const PathSel sel = path_sel();
     const TableArg &tab = s->impl.tab;
+    const size_t gws = round256(global_ws_bytes(tab, B));   // placed after the path's own scratch
     if (sel == PathSel::Generic) {
         *path = BwdPath::Generic;
         return (size_t)B * tab.H * tab.N * sizeof(float);
     }
     if (sel != PathSel::Flat && cached_plan(s, true, tab, B, dt, pl)) {
         *path = BwdPath::Resident;
-        return 0;
+        return gws;
     }
     *path = BwdPath::Flat;
-    return flat_bwd_scratch_bytes(tab, B);
+    return gws ? round256(flat_bwd_scratch_bytes(tab, B)) + gws : flat_bwd_scratch_bytes(tab, B);
 }
 
 fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
@@ -416,12 +440,22 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
                              fmt("workspace holds %zu bytes, %zu needed", ws_bytes, need));
     }
     if (fault("launch")) return set_error(FIBATT_ERR_CUDA, "injected launch failure (FIBATT_FAULT=launch)");
+    if (s->impl.tab.global0 && path == BwdPath::Generic)
+        return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=generic has no global first token");
     BwdArgs a{&s->impl.tab, B, dtype, Q, K, V, O, dO, LSE, dQ, dK, dV, static_cast<float *>(workspace),
               scale, stream};
+    if (s->impl.tab.global0) {
+        const size_t own = path == BwdPath::Flat ? round256(flat_bwd_scratch_bytes(s->impl.tab, B)) : 0;
+        a.gw = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + own);
+    }
 
-    cudaError_t e = path == BwdPath::Resident ? launch_bwd_resident(a, pl)
-                    : path == BwdPath::Flat   ? launch_bwd_flat(a)
-                                              : launch_bwd_generic(a);
+    cudaError_t e = cudaSuccess;
+    if (a.gw) e = launch_bwd_global_row(a);   // dQ_0 and the weights of the pairs (0, k)
+    if (e == cudaSuccess)
+        e = path == BwdPath::Resident ? launch_bwd_resident(a, pl)
+            : path == BwdPath::Flat   ? launch_bwd_flat(a)
+                                      : launch_bwd_generic(a);
+    if (e == cudaSuccess && a.gw) e = launch_bwd_global_col(a);   // dK_0, dV_0
     if (e != cudaSuccess) return cuda_error(e, "fibatt_bwd launch");
     return FIBATT_OK;
 }

@@ -27,6 +27,7 @@ struct TableArg {
     int32_t N;
     int32_t max_count;                 // max entries of one head
     int32_t max_abs;                   // max |offset| over all heads
+    int32_t global0;                   // token 0 global (row 0 and column 0 attended)
     int32_t start[kMaxHeads + 1];
     int32_t off[kMaxEntries];
 };
@@ -35,7 +36,8 @@ struct ResidentPlan;
 
 struct SupportImpl {
     TableArg tab;
-    std::vector<int64_t> pairs;        // |Omega_h| per head
+    std::vector<int64_t> pairs;        // |Omega_h| per head, banded part
+    std::vector<int64_t> global_pairs; // pairs the global token adds per head
 };
 
 // ---- launch accounting (fibatt_launch_count) -------------------------------
@@ -73,6 +75,7 @@ struct BwdArgs {
     float *Dws;                        // fp32 scratch: [B*H*N] (generic) or pair weights (flat)
     float scale;
     cudaStream_t stream;
+    float *gw = nullptr;               // global token: P_0k, dS_0k per (b, h) ([B*H][2][N] fp32)
 };
 
 // Shared-memory-resident kernels: one CTA per (b, h, query chunk); the
@@ -135,5 +138,12 @@ cudaError_t launch_bwd_flat(const BwdArgs &a);       // a.Dws: pair-weight scrat
 size_t flat_bwd_scratch_bytes(const TableArg &tab, int B);
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
+
+// Global first token (global_token.cu): the dense row of token 0 (forward,
+// after the banded kernel), its dense row before the banded backward, and
+// the column of key 0 after it.
+cudaError_t launch_fwd_global_row(const FwdArgs &a);
+cudaError_t launch_bwd_global_row(const BwdArgs &a);
+cudaError_t launch_bwd_global_col(const BwdArgs &a);
 
 }  // namespace fibatt

@@ -63,6 +63,8 @@ extern "C" fibatt_status fibatt_bwd_noalloc(fibatt_support_t s, int B, int D, fi
     fibatt_status st = check_bwd_args(s, B, D, dtype, Q, K, V, O, LSE, dO, scale, dQ, dK, dV);
     if (st != FIBATT_OK) return st;
     const TableArg &tab = support_table(s);
+    if (tab.global0)
+        return set_error(FIBATT_ERR_UNSUPPORTED, "fibatt_bwd_noalloc has no global first token; use fibatt_bwd");
     const size_t rows = (size_t)B * tab.H * tab.N;
     if (rows > kNoAllocRows) {
         char msg[200];

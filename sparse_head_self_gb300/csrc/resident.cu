@@ -196,11 +196,24 @@ __device__ __forceinline__ void round_range(const int *off, int N, int t0, int t
     te = max(tb, t1 - above);
 }
 
+// Whether the ascending offsets off[t0..t1) contain v (binary search).
+__device__ __forceinline__ bool table_has(const int *off, int t0, int t1, int v) {
+    while (t0 < t1) {
+        const int mid = (t0 + t1) >> 1;
+        const int o = off[mid];
+        if (o == v) return true;
+        if (o < v) t0 = mid + 1;
+        else t1 = mid;
+    }
+    return false;
+}
+
 // Round r of a unit: query rows [q0 + r R, q0 + r R + R) with R = 32 / G.
 template <typename T, int G, int UNROLL>
 __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, const PipeParams &p, const Unit &g,
                                           const uint8_t *sQ, const uint8_t *sK, ptrdiff_t vdelta, int r,
-                                          const LaneGeom<T, G> &lg) {
+                                          const LaneGeom<T, G> &lg, const uint8_t *sK0 = nullptr,
+                                          const uint8_t *sV0 = nullptr) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
     constexpr int R = 32 / G;
@@ -226,6 +239,20 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
     st.m = kMaxInit;
     st.l = 0.f;
     fwd_offsets<T, G, UNROLL>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
+    if (tab.global0) {
+        // global first token: key 0 for every query row j >= 1 whose band
+        // misses it (offset -j absent; the tables are symmetric)
+        const bool need = valid && j >= 1 && !table_has(off, g.t0, g.t1, j);
+        S kr;
+        kr.load(sK0, lg.c);
+        float s0 = group_sum<G>(q.dot(kr)) * p.scale_log2;
+        s0 = need ? s0 : -INFINITY;
+        softmax_raise(st, s0);
+        const float pr = fast_exp2(s0 - st.m);
+        st.l += pr;
+        kr.load(sV0, lg.c);
+        kr.axpy(pr, st.acc);
+    }
     if (valid) {
         const float inv = st.l > 0.f ? __frcp_rn(st.l) : 0.f;
 #pragma unroll
@@ -275,6 +302,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     grid_dep_launch();
 
     const size_t q_off = 0, k_off = (size_t)p.chunk * RB, v_off = k_off + (size_t)p.kv_cap * RB;
+    const size_t g0_off = v_off + (size_t)p.kv_cap * RB;   // K and V row 0 (global first token)
     if (warp == 0) {
         // producer: one lane streams every unit of this CTA into the ring and
         // keeps the next `prefetch` units warming in L2
@@ -292,12 +320,16 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)g.bh * tab.N;
             const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
-            mbar_expect_tx(&full_bar[s], qb + 2 * kvb);
+            mbar_expect_tx(&full_bar[s], qb + 2 * kvb + (tab.global0 ? 2u * RB : 0u));
             if (qb)   // a last-wave piece past the end of its chunk has no rows
                 bulk_g2s(st + q_off, static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, qb, &full_bar[s]);
             if (kvb) {
                 bulk_g2s(st + k_off, static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
                 bulk_g2s(st + v_off, static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
+            }
+            if (tab.global0) {   // key and value row 0, for the global first token
+                bulk_g2s(st + g0_off, static_cast<const T *>(p.K) + row0 * kHeadDim, RB, &full_bar[s]);
+                bulk_g2s(st + g0_off + RB, static_cast<const T *>(p.V) + row0 * kHeadDim, RB, &full_bar[s]);
             }
             if (i >= 1 && p.prefetch > 0) {
                 const int un = u + (p.stages + p.prefetch - 1) * gridDim.x;
@@ -326,7 +358,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const Unit g = unit_geometry(tab, p, u);
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         for (int r = wg; r < rpu; r += p.gwarps)
-            fwd_round<T, G, UNROLL>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg);
+            fwd_round<T, G, UNROLL>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
+                                    st + g0_off, st + g0_off + RB);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -368,7 +401,7 @@ fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
     const LaneGeom<T, G> lg;
     const int r = blockIdx.y * W + (threadIdx.x >> 5);
-    fwd_round<T, G, UNROLL>(tab, s_off, p, g, gQ, gK, vdelta, r, lg);
+    fwd_round<T, G, UNROLL>(tab, s_off, p, g, gQ, gK, vdelta, r, lg, gK, gK + vdelta);
 }
 
 // ---------------------------------------------------------------- backward
@@ -432,6 +465,7 @@ struct BwdParams {
     uint32_t stage_bytes;
     uint32_t scratch_off;   // byte offset of the P/dS scratch in dynamic smem
     int max_count;          // max table entries of one head (scratch rows)
+    const float *gw;        // global first token: P_0k, dS_0k ([B*H][2][N]), or NULL
 };
 
 // Phase A for one round of query rows, branch-free: the key row is clamped
@@ -488,6 +522,39 @@ __device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int
         qq.axpy(dS, dk);
         gg.axpy(P, dv);
     }
+}
+
+// Global first token, phase A: the pair (j, 0) for a query row j >= 1 whose
+// band misses key 0 (sK0: key row 0; value row 0 at sK0 + vdelta).
+template <typename T, int G>
+__device__ __forceinline__ void bwd_a_global(const int *off, int t0, int t1, int j, bool valid, const uint8_t *sK0,
+                                             ptrdiff_t vdelta, const Slice<T, G> &q, const Slice<T, G> &g, float Dj,
+                                             float lse2, float sl2, const LaneGeom<T, G> &lg, float2 (&dq)[32 / G]) {
+    const bool need = valid && j >= 1 && !table_has(off, t0, t1, j);
+    Slice<T, G> kk, vv;
+    kk.load(sK0, lg.c);
+    vv.load(sK0 + vdelta, lg.c);
+    const float s = group_sum<G>(q.dot(kk));
+    const float dp = group_sum<G>(g.dot(vv));
+    const float P = need ? fast_exp2(fmaf(s, sl2, -lse2)) : 0.f;
+    kk.axpy(P * (dp - Dj), dq);
+}
+
+// Global first token, phase B: the pair (0, k) for a key row k >= 1 whose
+// band misses query 0, with P_0k and dS_0k from the dense-row kernel (gw of
+// this (b, h)); sQ0: query row 0, its dO row at sQ0 + gdelta.
+template <typename T, int G>
+__device__ __forceinline__ void bwd_b_global(const int *off, int t0, int t1, int k, bool valid, const float *gw,
+                                             int N, const uint8_t *sQ0, ptrdiff_t gdelta, const LaneGeom<T, G> &lg,
+                                             float2 (&dk)[32 / G], float2 (&dv)[32 / G]) {
+    const bool need = valid && k >= 1 && !table_has(off, t0, t1, k);
+    const float P = need ? gw[k] : 0.f;
+    const float dS = need ? gw[N + k] : 0.f;
+    Slice<T, G> qq, gg;
+    qq.load(sQ0, lg.c);
+    gg.load(sQ0 + gdelta, lg.c);
+    qq.axpy(dS, dk);
+    gg.axpy(P, dv);
 }
 
 // MAXT: threads per CTA the register budget is sized for (65536 / MAXT each).
@@ -589,7 +656,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
             bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg,
                                 scrP, scrS, dq);
-            if (valid) {
+            if (tab.global0)
+                bwd_a_global<T, G>(s_off, t0, t1, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg, dq);
+            if (valid && !(tab.global0 && j == 0)) {   // dQ_0: dense-row kernel
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
                 S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
@@ -609,7 +678,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
             bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (ptrdiff_t)(3 * tens), lg, scrP, scrS, dk,
                                 dv);
-            if (valid) {
+            if (tab.global0)
+                bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)u * 2 * N, N, sQ, (ptrdiff_t)(3 * tens),
+                                   lg, dk, dv);
+            if (valid && !(tab.global0 && k == 0)) {   // dK_0, dV_0: column kernel
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
                 S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
@@ -660,7 +732,8 @@ __device__ __forceinline__ void bwd_flat_a_round(const TableArg &tab, const BwdP
     for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
     bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, scrP, scrS,
                         dq);
-    if (valid) {
+    if (tab.global0) bwd_a_global<T, G>(s_off, t0, t1, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, dq);
+    if (valid && !(tab.global0 && j == 0)) {
 #pragma unroll
         for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
         S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
@@ -718,7 +791,8 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
 #pragma unroll
     for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
     bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, gQ, gdelta, lg, scrP, scrS, dk, dv);
-    if (valid) {
+    if (tab.global0) bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)bh * 2 * N, N, gQ, gdelta, lg, dk, dv);
+    if (valid && !(tab.global0 && k == 0)) {
 #pragma unroll
         for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
         S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
@@ -791,7 +865,7 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     // the windows are too wide for this kernel.
     {
         const int qs_min = (N + R - 1) / R;
-        const size_t smallest = (size_t)R * RB + 2 * (size_t)window_cap(tab, qs_min, R) * RB;
+        const size_t smallest = (size_t)R * RB + 2 * (size_t)window_cap(tab, qs_min, R) * RB + 2 * RB;
         if (smallest > budget) return false;
     }
     int chunk = 0, kv_cap = 0;
@@ -801,7 +875,7 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
         chunk = ((N + qsplit - 1) / qsplit + R - 1) / R * R;
         const int qs = (N + chunk - 1) / chunk;
         kv_cap = window_cap(tab, qs, chunk);
-        stage = ((size_t)chunk * RB + 2 * (size_t)kv_cap * RB + 127) / 128 * 128;
+        stage = ((size_t)chunk * RB + 2 * (size_t)kv_cap * RB + (tab.global0 ? 2 * RB : 0) + 127) / 128 * 128;
         if (env || 3 * stage <= budget || chunk <= R) {
             qsplit = qs;
             break;
@@ -941,7 +1015,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     }
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 units, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
-                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count)};
+                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -954,7 +1028,7 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count)};
+                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw};
     const dim3 grid((unsigned)count, (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
     float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N

@@ -104,6 +104,34 @@ def test_distance_support_matches_oracle():
             assert sup.pairs[h] == oracle.support_size(N, head)
 
 
+def test_global_token_pair_counts_match_oracle():
+    for name in ("tiny", "vitb", "vitb_nodiag"):
+        wl = WORKLOADS[name]
+        sup = api.Support.wythoff(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag)
+        banded = sup.pairs
+        sup.set_global_token(True)
+        heads = oracle.wythoff_heads(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag, global_token=True)
+        assert sup.pairs == [oracle.support_size(wl.N, h) for h in heads]
+        # the tables keep describing the banded part
+        assert sup.head_offsets() == [[int(x) for x in oracle.signed_table(wl.N, h)] for h in heads]
+        sup.set_global_token(False)
+        assert sup.pairs == banded
+    d = [[], [3, 9]]
+    sup = api.Support.from_distances(12, d, False).set_global_token(True)
+    assert sup.pairs == [oracle.support_size(12, oracle.Head(x, 12, False, global_token=True)) for x in d]
+
+
+def test_global_token_unsupported_paths_fail_before_launch(monkeypatch):
+    L = _native.lib()
+    sup = api.Support.wythoff(3, 65, 5, 65, True).set_global_token(True)
+    fake, lse = 1 << 20, 1 << 21   # never dereferenced: both calls fail their checks first
+    monkeypatch.setenv("FIBATT_PATH", "generic")
+    assert L.fibatt_fwd(sup.handle, 1, 64, 0, fake, fake, fake, 0.125, fake, lse, None) == 2
+    assert "global" in L.fibatt_last_error().decode()
+    assert L.fibatt_bwd_noalloc(sup.handle, 1, 64, 0, fake, fake, fake, fake, lse, fake, 0.1, fake, fake, fake,
+                                None) == 2
+
+
 def test_permutation_reorders_heads():
     base = api.Support.wythoff(4, 100, 5, 100, True)
     perm = [2, 0, 3, 1]

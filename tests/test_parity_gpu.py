@@ -10,8 +10,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (assert_close, make_inputs, oracle_heads, pick_rows, support_for,
-                         to_dev)
+from gpu_helpers import (assert_close, assert_close_global, make_inputs, oracle_heads, pick_rows,
+                         support_for, to_dev)
 from sparse_head_self_gb300 import api
 from sparse_head_self_gb300.inputs import WORKLOADS, Workload
 
@@ -255,6 +255,63 @@ def test_chained_calls_match_synchronised_calls(kernel_path):
     for i in range(6):
         for a, b in zip(grads[i], ref[i % 3][2:]):
             assert torch.equal(a, b)
+
+
+# ------------------------------------------------- global first token (CLS)
+
+def _global_fwd_bwd(wl, seed, heads_subset=None):
+    q, k, v, do = make_inputs(wl, seed)
+    sup = support_for(wl, global_token=True)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    torch.cuda.synchronize()
+    heads = oracle_heads(wl, global_token=True)
+    hs = range(wl.H) if heads_subset is None else heads_subset
+    for b in range(wl.B):
+        for h in hs:
+            Or, Lr = oracle.fwd_head(q[b, h], k[b, h], v[b, h], heads[h], wl.scale)
+            assert_close_global(f"O b{b} h{h}", O[b, h].float().cpu(), Or, wl.dtype)
+            assert_close_global(f"LSE b{b} h{h}", L[b, h].cpu(), Lr, wl.dtype, lse=True)
+            rQ, rK, rV = oracle.bwd_head(q[b, h], k[b, h], v[b, h], do[b, h], heads[h], wl.scale)
+            assert_close_global(f"dQ b{b} h{h}", dQ[b, h].float().cpu(), rQ, wl.dtype)
+            assert_close_global(f"dK b{b} h{h}", dK[b, h].float().cpu(), rK, wl.dtype)
+            assert_close_global(f"dV b{b} h{h}", dV[b, h].float().cpu(), rV, wl.dtype)
+
+
+@pytest.mark.parametrize("kernel_path", ["resident", "flat"], indirect=True)
+def test_global_token_tiny_fp32(kernel_path):
+    _global_fwd_bwd(WORKLOADS["tiny"], 21)
+
+
+@pytest.mark.parametrize("kernel_path", ["resident", "flat"], indirect=True)
+@pytest.mark.parametrize("name", ["vitb", "vitb_nodiag"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_global_token_vitb_shape(name, dtype, kernel_path):
+    _global_fwd_bwd(Workload(**{**WORKLOADS[name].__dict__, "B": 2, "dtype": dtype}), 22)
+
+
+@pytest.mark.parametrize("kernel_path", ["resident", "flat", "auto"], indirect=True)
+@pytest.mark.parametrize("N", [1, 2, 3, 9, 40])
+def test_global_token_edge_sizes(N, kernel_path):
+    wl = Workload("edge", 2, 3, N, 64, "f32", 1, N, False, True)
+    _global_fwd_bwd(wl, 23)
+
+
+def test_global_token_video_two_heads():
+    wl = WORKLOADS["video"].with_batch(1)
+    _global_fwd_bwd(wl, 24, heads_subset=(0, wl.H - 1))
+
+
+def test_global_token_only_support_gives_v0():
+    # no distances, no diagonal: every query but token 0 attends key 0 alone
+    N, B = 50, 2
+    sup = api.Support.from_distances(N, [[], []], False).set_global_token(True)
+    wl = Workload("g", B, 2, N, 64, "f32", 2, 2, False, True)
+    q, k, v, _ = make_inputs(wl, 25, with_grad=False)
+    O, L = api.fwd(sup, *to_dev(q, k, v), wl.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(O[:, :, 1:].cpu(), v[:, :, :1].expand(B, 2, N - 1, 64))
 
 
 # ----------------------------------------------- full sizes, bench launches
