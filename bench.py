@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="vitb")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--global-token", action="store_true",
+                   help="token 0 global in every head (README Algorithm 2's class token)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args(argv)
@@ -189,7 +191,8 @@ class ClockSampler:
 class Step:
     """Raw C-ABI calls for one step on one rotating buffer set."""
 
-    def __init__(self, wl, dev, rotate: int, seed: int = 0):
+    def __init__(self, wl, dev, rotate: int, seed: int = 0, global_token: bool = False):
+        self.global_token = global_token
         self.lib = _native.lib()
         self.wl = wl
         H = wl.H
@@ -202,7 +205,7 @@ class Step:
         q, k, v, do = make_inputs(wl, seed)
         self.host = (q, k, v, do)
         self.sets = []
-        sup = api.Support.wythoff(H, wl.N, wl.w_min, wl.w_max, wl.diag)
+        sup = api.Support.wythoff(H, wl.N, wl.w_min, wl.w_max, wl.diag).set_global_token(global_token)
         self.pairs = sup.total_pairs(wl.B)
         ws_bytes = sup.bwd_workspace_bytes(wl.B)
         for r in range(rotate):
@@ -226,6 +229,7 @@ class Step:
         h = ctypes.c_void_p()
         _native.check(L.fibatt_support_build(wl.H, wl.N, self.a, self.b, self.w, int(wl.diag),
                                              ctypes.byref(h)))
+        _native.check(L.fibatt_support_set_global_token(h, int(self.global_token)))
         if ev is not None:
             ev[0].record()
         _native.check(L.fibatt_fwd(h, wl.B, wl.D, self.dt, p["Q"], p["K"], p["V"], wl.scale, p["O"],
@@ -247,6 +251,7 @@ class Step:
         h = ctypes.c_void_p()
         _native.check(L.fibatt_support_build(wl.H, wl.N, self.a, self.b, self.w, int(wl.diag),
                                              ctypes.byref(h)))
+        _native.check(L.fibatt_support_set_global_token(h, int(self.global_token)))
         out = []
         for kind in ("fwd", "bwd"):
             for i in range(3):
@@ -285,7 +290,7 @@ def run_e2e(step: Step, dev, steps: int):
     d2h = sum(x.numel() * x.element_size() for x in outs.values())
 
     def one():
-        sup = api.Support.wythoff(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag)
+        sup = api.Support.wythoff(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag).set_global_token(step.global_token)
         for n, x in zip(("Q", "K", "V", "dO"), (q, k, v, do)):
             t[n].copy_(x, non_blocking=True)
         api.fwd(sup, t["Q"], t["K"], t["V"], wl.scale, O=t["O"], LSE=t["LSE"])
@@ -308,16 +313,36 @@ def run_e2e(step: Step, dev, steps: int):
     return ms, h2d, d2h
 
 
-def cpu_baseline(wl, target_s: float):
+def _oracle_heads(wl, global_token: bool):
+    import oracle
+    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
+    return [oracle.Head.fibottention(*oracle.wythoff_row(i + 1), w[i], wl.diag, global_token)
+            for i in range(wl.H)]
+
+
+def _row_pairs(N, table, global_token, rows):
+    """Attended pairs of the listed query rows: the banded ones read off the
+    signed table, plus what the global first token adds (every key for row 0,
+    key 0 for a row whose band misses it)."""
+    offs = [int(d) for d in table]
+    n = 0
+    for j in rows:
+        band = sum(1 for d in offs if 0 <= j + d < N)
+        if global_token:
+            band = N if j == 0 else band + (0 if -j in offs else 1)
+        n += band
+    return n
+
+
+def cpu_baseline(wl, target_s: float, global_token: bool = False):
     """The fp64 oracle as it stands, on the host cores, on a bounded sample of
     the workload: forward and backward of whole (b, h) heads, all rows."""
     import oracle
     cores = oracle.set_threads(oracle.max_threads())
     q, k, v, do = make_inputs(wl.with_batch(1), 0)
-    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
-    heads = [oracle.Head.fibottention(*oracle.wythoff_row(i + 1), w[i], wl.diag) for i in range(wl.H)]
+    heads = _oracle_heads(wl, global_token)
     pairs_head = [oracle.support_size(wl.N, hd) if wl.N <= 2048 else
-                  sum(wl.N - abs(int(d)) for d in oracle.signed_table(wl.N, hd)) for hd in heads]
+                  _row_pairs(wl.N, oracle.signed_table(wl.N, hd), global_token, range(wl.N)) for hd in heads]
     done_pairs, done_heads, t0 = 0, 0, time.perf_counter()
     while True:
         h = done_heads % wl.H
@@ -342,11 +367,11 @@ def gb300_arm(args):
     init_dist(world, "nccl")
     wl = WORKLOADS[args.workload]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    probe = Step(wl, dev, 1)
+    probe = Step(wl, dev, 1, global_token=args.global_token)
     per_set = probe.bytes_per_set()
     rotate = max(2, math.ceil(3 * l2 / per_set) + 1)
     del probe
-    step = Step(wl, dev, rotate)
+    step = Step(wl, dev, rotate, global_token=args.global_token)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
@@ -402,7 +427,8 @@ def gb300_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": (f"{wl.name}: B={wl.B} H={wl.H} N={wl.N} d={wl.D} {wl.dtype}, "
                                 f"Wythoff rows 1..{wl.H}, w {wl.w_min}..{wl.w_max}, "
-                                f"diag={'on' if wl.diag else 'off'}"),
+                                f"diag={'on' if wl.diag else 'off'}"
+                                + (", global token 0" if args.global_token else "")),
                    "B_per_gpu": wl.B, "H": wl.H, "N": wl.N,
                    "step": "support build + fwd + bwd (all hot-path rows)",
                    "pairs_per_step_per_gpu": step.pairs,
@@ -426,7 +452,7 @@ def gb300_arm(args):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, args.global_token)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -446,12 +472,11 @@ def reference_arm(args):
     wl = WORKLOADS[args.workload]
     cores = oracle.set_threads(oracle.max_threads())
     q, k, v, do = make_inputs(wl.with_batch(1), 0)
-    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
-    heads = [oracle.Head.fibottention(*oracle.wythoff_row(i + 1), w[i], wl.diag) for i in range(wl.H)]
+    heads = _oracle_heads(wl, args.global_token)
     tables = [oracle.signed_table(wl.N, hd) for hd in heads]
 
     def row_pairs(h, rows):
-        return sum(1 for j in rows for d in tables[h] if 0 <= j + int(d) < wl.N)
+        return _row_pairs(wl.N, tables[h], args.global_token, rows)
 
     def one(i, nrows):
         h = i % wl.H

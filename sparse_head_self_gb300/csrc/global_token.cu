@@ -12,15 +12,16 @@
 //   bwd_global_col_kernel   dK_0, dV_0 over every query (the whole column of
 //                           key 0, every query attends it)
 //
-// One block of kGtWarps warps per (b, h); a warp takes one key (or query) row
-// at a time, two dims per lane, dot products reduced across the warp.
+// One block of NW warps per (b, h) (8 for short sequences, 32 for long ones);
+// a warp takes kGtRows key (or query) rows at a time (their loads issued
+// together), two dims per lane, dot products reduced across the warp.
 #include "device_common.cuh"
 #include "fibatt_internal.h"
 
 namespace fibatt {
 namespace {
 
-constexpr int kGtWarps = 8;
+constexpr int kGtRows = 4;   // rows per warp step
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -45,6 +46,7 @@ __device__ __forceinline__ void store_pair(float *row, int lane, float2 v) {
 
 // Merge the warps' (m, l, acc) of a softmax taken in log2 units into the
 // block's: returns (acc / l for this lane's two dims, m + log2 l) in warp 0.
+template <int NW>
 __device__ __forceinline__ void merge_warps(float m, float l, float2 acc, float *s_m, float *s_l, float2 *s_acc,
                                             int warp, int lane, float2 *out, float *lse2) {
     if (lane == 0) {
@@ -55,10 +57,10 @@ __device__ __forceinline__ void merge_warps(float m, float l, float2 acc, float 
     __syncthreads();
     if (warp == 0) {
         float M = -INFINITY;
-        for (int w = 0; w < kGtWarps; ++w) M = fmaxf(M, s_m[w]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
         float L = 0.f;
         float2 A = make_float2(0.f, 0.f);
-        for (int w = 0; w < kGtWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const float f = s_l[w] > 0.f ? exp2f(s_m[w] - M) : 0.f;
             L += f * s_l[w];
             A.x += f * s_acc[w * 32 + lane].x;
@@ -70,12 +72,12 @@ __device__ __forceinline__ void merge_warps(float m, float l, float2 acc, float 
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kGtWarps * 32)
+template <typename T, int NW>
+__global__ void __launch_bounds__(NW * 32)
 fwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                       float scale_log2, T *__restrict__ O, float *__restrict__ LSE) {
-    __shared__ float s_m[kGtWarps], s_l[kGtWarps];
-    __shared__ float2 s_acc[kGtWarps * 32];
+    __shared__ float s_m[NW], s_l[NW];
+    __shared__ float2 s_acc[NW * 32];
     grid_dep_wait();
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,25 +85,41 @@ fwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
     const float2 q = row_pair(Q + base, lane);
     float m = -INFINITY, l = 0.f;
     float2 acc = make_float2(0.f, 0.f);
-    for (int k = warp; k < N; k += kGtWarps) {
-        const float2 kk = row_pair(K + base + (size_t)k * kHeadDim, lane);
-        const float s = warp_sum(fmaf(q.x, kk.x, q.y * kk.y)) * scale_log2;
-        if (s > m) {   // warp-uniform
-            const float a = exp2f(m - s);
+    for (int k0 = warp * kGtRows; k0 < N; k0 += NW * kGtRows) {
+        float2 kk[kGtRows], vv[kGtRows];
+        float s[kGtRows];
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const int k = min(k0 + i, N - 1);
+            kk[i] = row_pair(K + base + (size_t)k * kHeadDim, lane);
+            vv[i] = row_pair(V + base + (size_t)k * kHeadDim, lane);
+        }
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const float x = warp_sum(fmaf(q.x, kk[i].x, q.y * kk[i].y)) * scale_log2;
+            s[i] = k0 + i < N ? x : -INFINITY;
+        }
+        float mb = s[0];
+#pragma unroll
+        for (int i = 1; i < kGtRows; ++i) mb = fmaxf(mb, s[i]);
+        if (mb > m) {   // warp-uniform
+            const float a = exp2f(m - mb);
             l *= a;
             acc.x *= a;
             acc.y *= a;
-            m = s;
+            m = mb;
         }
-        const float p = exp2f(s - m);
-        l += p;
-        const float2 vv = row_pair(V + base + (size_t)k * kHeadDim, lane);
-        acc.x = fmaf(p, vv.x, acc.x);
-        acc.y = fmaf(p, vv.y, acc.y);
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const float p = exp2f(s[i] - m);
+            l += p;
+            acc.x = fmaf(p, vv[i].x, acc.x);
+            acc.y = fmaf(p, vv[i].y, acc.y);
+        }
     }
     float2 o;
     float lse2;
-    merge_warps(m, l, acc, s_m, s_l, s_acc, warp, lane, &o, &lse2);
+    merge_warps<NW>(m, l, acc, s_m, s_l, s_acc, warp, lane, &o, &lse2);
     if (warp == 0) {
         store_pair(O + base, lane, o);
         if (lane == 0) LSE[(size_t)blockIdx.x * N] = lse2 * kLn2;
@@ -109,12 +127,12 @@ fwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
 }
 
 // gw: [B*H][2][N] fp32: P_0k, then dS_0k.
-template <typename T>
-__global__ void __launch_bounds__(kGtWarps * 32)
+template <typename T, int NW>
+__global__ void __launch_bounds__(NW * 32)
 bwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                       const T *__restrict__ O, const float *__restrict__ LSE, const T *__restrict__ dO,
                       float scale, float scale_log2, T *__restrict__ dQ, float *__restrict__ gw) {
-    __shared__ float2 s_acc[kGtWarps * 32];
+    __shared__ float2 s_acc[NW * 32];
     grid_dep_wait();
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,25 +142,34 @@ bwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
     const float D0 = warp_sum(fmaf(g.x, o.x, g.y * o.y));
     const float lse2 = LSE[(size_t)blockIdx.x * N] * kLog2e;
     float2 dq = make_float2(0.f, 0.f);
-    for (int k = warp; k < N; k += kGtWarps) {
-        const float2 kk = row_pair(K + base + (size_t)k * kHeadDim, lane);
-        const float2 vv = row_pair(V + base + (size_t)k * kHeadDim, lane);
-        const float s = warp_sum(fmaf(q.x, kk.x, q.y * kk.y));
-        const float dp = warp_sum(fmaf(g.x, vv.x, g.y * vv.y));
-        const float P = exp2f(fmaf(s, scale_log2, -lse2));
-        const float dS = P * (dp - D0);
-        if (lane == 0) {
-            gP[k] = P;
-            gS[k] = dS;
+    for (int k0 = warp * kGtRows; k0 < N; k0 += NW * kGtRows) {
+        float2 kk[kGtRows], vv[kGtRows];
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const int k = min(k0 + i, N - 1);
+            kk[i] = row_pair(K + base + (size_t)k * kHeadDim, lane);
+            vv[i] = row_pair(V + base + (size_t)k * kHeadDim, lane);
         }
-        dq.x = fmaf(dS, kk.x, dq.x);
-        dq.y = fmaf(dS, kk.y, dq.y);
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const float s = warp_sum(fmaf(q.x, kk[i].x, q.y * kk[i].y));
+            const float dp = warp_sum(fmaf(g.x, vv[i].x, g.y * vv[i].y));
+            const bool in = k0 + i < N;
+            const float P = in ? exp2f(fmaf(s, scale_log2, -lse2)) : 0.f;
+            const float dS = P * (dp - D0);
+            if (lane == 0 && in) {
+                gP[k0 + i] = P;
+                gS[k0 + i] = dS;
+            }
+            dq.x = fmaf(dS, kk[i].x, dq.x);
+            dq.y = fmaf(dS, kk[i].y, dq.y);
+        }
     }
     s_acc[warp * 32 + lane] = dq;
     __syncthreads();
     if (warp == 0) {
         float2 a = make_float2(0.f, 0.f);
-        for (int w = 0; w < kGtWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             a.x += s_acc[w * 32 + lane].x;
             a.y += s_acc[w * 32 + lane].y;
         }
@@ -150,37 +177,49 @@ bwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kGtWarps * 32)
+template <typename T, int NW>
+__global__ void __launch_bounds__(NW * 32)
 bwd_global_col_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                       const T *__restrict__ O, const float *__restrict__ LSE, const T *__restrict__ dO,
                       float scale, float scale_log2, T *__restrict__ dK, T *__restrict__ dV) {
-    __shared__ float2 s_k[kGtWarps * 32], s_v[kGtWarps * 32];
+    __shared__ float2 s_k[NW * 32], s_v[NW * 32];
     grid_dep_wait();
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t base = (size_t)blockIdx.x * N * kHeadDim;
     const float2 k0 = row_pair(K + base, lane), v0 = row_pair(V + base, lane);
     float2 dk = make_float2(0.f, 0.f), dv = make_float2(0.f, 0.f);
-    for (int j = warp; j < N; j += kGtWarps) {
-        const size_t r = base + (size_t)j * kHeadDim;
-        const float2 q = row_pair(Q + r, lane), g = row_pair(dO + r, lane), o = row_pair(O + r, lane);
-        const float s = warp_sum(fmaf(q.x, k0.x, q.y * k0.y));
-        const float dp = warp_sum(fmaf(g.x, v0.x, g.y * v0.y));
-        const float Dj = warp_sum(fmaf(g.x, o.x, g.y * o.y));
-        const float P = exp2f(fmaf(s, scale_log2, -LSE[(size_t)blockIdx.x * N + j] * kLog2e));
-        const float dS = P * (dp - Dj);
-        dk.x = fmaf(dS, q.x, dk.x);
-        dk.y = fmaf(dS, q.y, dk.y);
-        dv.x = fmaf(P, g.x, dv.x);
-        dv.y = fmaf(P, g.y, dv.y);
+    for (int j0 = warp * kGtRows; j0 < N; j0 += NW * kGtRows) {
+        float2 q[kGtRows], g[kGtRows], o[kGtRows];
+        float lse[kGtRows];
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const int j = min(j0 + i, N - 1);
+            const size_t r = base + (size_t)j * kHeadDim;
+            q[i] = row_pair(Q + r, lane);
+            g[i] = row_pair(dO + r, lane);
+            o[i] = row_pair(O + r, lane);
+            lse[i] = LSE[(size_t)blockIdx.x * N + j];
+        }
+#pragma unroll
+        for (int i = 0; i < kGtRows; ++i) {
+            const float s = warp_sum(fmaf(q[i].x, k0.x, q[i].y * k0.y));
+            const float dp = warp_sum(fmaf(g[i].x, v0.x, g[i].y * v0.y));
+            const float Dj = warp_sum(fmaf(g[i].x, o[i].x, g[i].y * o[i].y));
+            const float P = j0 + i < N ? exp2f(fmaf(s, scale_log2, -lse[i] * kLog2e)) : 0.f;
+            const float dS = P * (dp - Dj);
+            dk.x = fmaf(dS, q[i].x, dk.x);
+            dk.y = fmaf(dS, q[i].y, dk.y);
+            dv.x = fmaf(P, g[i].x, dv.x);
+            dv.y = fmaf(P, g[i].y, dv.y);
+        }
     }
     s_k[warp * 32 + lane] = dk;
     s_v[warp * 32 + lane] = dv;
     __syncthreads();
     if (warp == 0) {
         float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
-        for (int w = 0; w < kGtWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             a.x += s_k[w * 32 + lane].x;
             a.y += s_k[w * 32 + lane].y;
             b.x += s_v[w * 32 + lane].x;
@@ -191,11 +230,11 @@ bwd_global_col_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
     }
 }
 
-template <typename T>
+template <typename T, int NW>
 cudaError_t fwd_global(const FwdArgs &a) {
     const TableArg &tab = *a.tab;
-    const cudaError_t e = launch_kernel(fwd_global_row_kernel<T>, dim3((unsigned)(a.B * tab.H)),
-                                        dim3(kGtWarps * 32), 0, a.stream, pdl_enabled(), (int)tab.N,
+    const cudaError_t e = launch_kernel(fwd_global_row_kernel<T, NW>, dim3((unsigned)(a.B * tab.H)),
+                                        dim3(NW * 32), 0, a.stream, pdl_enabled(), (int)tab.N,
                                         static_cast<const T *>(a.Q), static_cast<const T *>(a.K),
                                         static_cast<const T *>(a.V), a.scale * kLog2e, static_cast<T *>(a.O),
                                         a.LSE);
@@ -203,18 +242,18 @@ cudaError_t fwd_global(const FwdArgs &a) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, int NW>
 cudaError_t bwd_global(const BwdArgs &a, bool row) {
     const TableArg &tab = *a.tab;
-    const dim3 grid((unsigned)(a.B * tab.H)), block(kGtWarps * 32);
+    const dim3 grid((unsigned)(a.B * tab.H)), block(NW * 32);
     cudaError_t e;
     if (row)
-        e = launch_kernel(bwd_global_row_kernel<T>, grid, block, 0, a.stream, pdl_enabled(), (int)tab.N,
+        e = launch_kernel(bwd_global_row_kernel<T, NW>, grid, block, 0, a.stream, pdl_enabled(), (int)tab.N,
                           static_cast<const T *>(a.Q), static_cast<const T *>(a.K), static_cast<const T *>(a.V),
                           static_cast<const T *>(a.O), a.LSE, static_cast<const T *>(a.dO), a.scale,
                           a.scale * kLog2e, static_cast<T *>(a.dQ), a.gw);
     else
-        e = launch_kernel(bwd_global_col_kernel<T>, grid, block, 0, a.stream, pdl_enabled(), (int)tab.N,
+        e = launch_kernel(bwd_global_col_kernel<T, NW>, grid, block, 0, a.stream, pdl_enabled(), (int)tab.N,
                           static_cast<const T *>(a.Q), static_cast<const T *>(a.K), static_cast<const T *>(a.V),
                           static_cast<const T *>(a.O), a.LSE, static_cast<const T *>(a.dO), a.scale,
                           a.scale * kLog2e, static_cast<T *>(a.dK), static_cast<T *>(a.dV));
@@ -224,16 +263,23 @@ cudaError_t bwd_global(const BwdArgs &a, bool row) {
 
 }  // namespace
 
+// 8 warps while a block's rows fit in a few steps, 32 beyond
+constexpr int kGtShortN = 8 * kGtRows * 8;
+
 cudaError_t launch_fwd_global_row(const FwdArgs &a) {
-    return a.dtype == FIBATT_F32 ? fwd_global<float>(a) : fwd_global<__nv_bfloat16>(a);
+    const bool wide = a.tab->N > kGtShortN;
+    if (a.dtype == FIBATT_F32) return wide ? fwd_global<float, 32>(a) : fwd_global<float, 8>(a);
+    return wide ? fwd_global<__nv_bfloat16, 32>(a) : fwd_global<__nv_bfloat16, 8>(a);
 }
 
-cudaError_t launch_bwd_global_row(const BwdArgs &a) {
-    return a.dtype == FIBATT_F32 ? bwd_global<float>(a, true) : bwd_global<__nv_bfloat16>(a, true);
+static cudaError_t bwd_global_any(const BwdArgs &a, bool row) {
+    const bool wide = a.tab->N > kGtShortN;
+    if (a.dtype == FIBATT_F32) return wide ? bwd_global<float, 32>(a, row) : bwd_global<float, 8>(a, row);
+    return wide ? bwd_global<__nv_bfloat16, 32>(a, row) : bwd_global<__nv_bfloat16, 8>(a, row);
 }
 
-cudaError_t launch_bwd_global_col(const BwdArgs &a) {
-    return a.dtype == FIBATT_F32 ? bwd_global<float>(a, false) : bwd_global<__nv_bfloat16>(a, false);
-}
+cudaError_t launch_bwd_global_row(const BwdArgs &a) { return bwd_global_any(a, true); }
+
+cudaError_t launch_bwd_global_col(const BwdArgs &a) { return bwd_global_any(a, false); }
 
 }  // namespace fibatt

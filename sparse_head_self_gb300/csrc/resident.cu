@@ -209,7 +209,7 @@ __device__ __forceinline__ bool table_has(const int *off, int t0, int t1, int v)
 }
 
 // Round r of a unit: query rows [q0 + r R, q0 + r R + R) with R = 32 / G.
-template <typename T, int G, int UNROLL>
+template <typename T, int G, int UNROLL, bool GT = false>
 __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, const PipeParams &p, const Unit &g,
                                           const uint8_t *sQ, const uint8_t *sK, ptrdiff_t vdelta, int r,
                                           const LaneGeom<T, G> &lg, const uint8_t *sK0 = nullptr,
@@ -239,7 +239,7 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
     st.m = kMaxInit;
     st.l = 0.f;
     fwd_offsets<T, G, UNROLL>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
-    if (tab.global0) {
+    if constexpr (GT) {
         // global first token: key 0 for every query row j >= 1 whose band
         // misses it (offset -j absent; the tables are symmetric)
         const bool need = valid && j >= 1 && !table_has(off, g.t0, g.t1, j);
@@ -276,7 +276,7 @@ __device__ __forceinline__ void prefetch_unit(const TableArg &tab, const PipePar
     }
 }
 
-template <typename T, int G, int UNROLL, int MAXT>
+template <typename T, int G, int UNROLL, int MAXT, bool GT = false>
 __global__ void __launch_bounds__(MAXT, 1)
 fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     using S = Slice<T, G>;
@@ -320,14 +320,14 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)g.bh * tab.N;
             const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
-            mbar_expect_tx(&full_bar[s], qb + 2 * kvb + (tab.global0 ? 2u * RB : 0u));
+            mbar_expect_tx(&full_bar[s], qb + 2 * kvb + (GT ? 2u * RB : 0u));
             if (qb)   // a last-wave piece past the end of its chunk has no rows
                 bulk_g2s(st + q_off, static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, qb, &full_bar[s]);
             if (kvb) {
                 bulk_g2s(st + k_off, static_cast<const T *>(p.K) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
                 bulk_g2s(st + v_off, static_cast<const T *>(p.V) + (row0 + g.lo) * kHeadDim, kvb, &full_bar[s]);
             }
-            if (tab.global0) {   // key and value row 0, for the global first token
+            if (GT) {   // key and value row 0, for the global first token
                 bulk_g2s(st + g0_off, static_cast<const T *>(p.K) + row0 * kHeadDim, RB, &full_bar[s]);
                 bulk_g2s(st + g0_off + RB, static_cast<const T *>(p.V) + row0 * kHeadDim, RB, &full_bar[s]);
             }
@@ -358,7 +358,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const Unit g = unit_geometry(tab, p, u);
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         for (int r = wg; r < rpu; r += p.gwarps)
-            fwd_round<T, G, UNROLL>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
+            fwd_round<T, G, UNROLL, GT>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
                                     st + g0_off, st + g0_off + RB);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -374,7 +374,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
 // (b, h); warp w of block y takes round y * kFlatWarps + w.
 constexpr int kFlatWarps = 4;   // 128-thread blocks measured fastest (4 to 32 warps tried)
 
-template <typename T, int G, int UNROLL, int W = kFlatWarps>
+template <typename T, int G, int UNROLL, int W = kFlatWarps, bool GT = false>
 __global__ void __launch_bounds__(W * 32)
 fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     __shared__ int s_off[kMaxEntries];
@@ -401,7 +401,7 @@ fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
     const LaneGeom<T, G> lg;
     const int r = blockIdx.y * W + (threadIdx.x >> 5);
-    fwd_round<T, G, UNROLL>(tab, s_off, p, g, gQ, gK, vdelta, r, lg, gK, gK + vdelta);
+    fwd_round<T, G, UNROLL, GT>(tab, s_off, p, g, gQ, gK, vdelta, r, lg, gK, gK + vdelta);
 }
 
 // ---------------------------------------------------------------- backward
@@ -558,7 +558,7 @@ __device__ __forceinline__ void bwd_b_global(const int *off, int t0, int t1, int
 }
 
 // MAXT: threads per CTA the register budget is sized for (65536 / MAXT each).
-template <typename T, int G, int MAXT>
+template <typename T, int G, int MAXT, bool GT = false>
 __global__ void __launch_bounds__(MAXT, 1)
 bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     using S = Slice<T, G>;
@@ -656,9 +656,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
             bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg,
                                 scrP, scrS, dq);
-            if (tab.global0)
+            if constexpr (GT)
                 bwd_a_global<T, G>(s_off, t0, t1, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg, dq);
-            if (valid && !(tab.global0 && j == 0)) {   // dQ_0: dense-row kernel
+            if (valid && !(GT && j == 0)) {   // dQ_0: dense-row kernel
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
                 S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
@@ -678,10 +678,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
             bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (ptrdiff_t)(3 * tens), lg, scrP, scrS, dk,
                                 dv);
-            if (tab.global0)
+            if constexpr (GT)
                 bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)u * 2 * N, N, sQ, (ptrdiff_t)(3 * tens),
                                    lg, dk, dv);
-            if (valid && !(tab.global0 && k == 0)) {   // dK_0, dV_0: column kernel
+            if (valid && !(GT && k == 0)) {   // dK_0, dV_0: column kernel
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
                 S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
@@ -699,7 +699,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 // pair weights P and dS in a global scratch [b, h][2][max_count][N] (phase A
 // writes the pairs in range, phase B reads exactly those).  Phase A: dQ;
 // phase B: dK, dV.  Block: kFlatWarps warps of one (b, h), one round each.
-template <typename T, int G>
+template <typename T, int G, bool GT>
 __device__ __forceinline__ void bwd_flat_a_round(const TableArg &tab, const BwdParams &p, const int *s_off,
                                                  float *scr, int bh, int r) {
     using S = Slice<T, G>;
@@ -732,15 +732,15 @@ __device__ __forceinline__ void bwd_flat_a_round(const TableArg &tab, const BwdP
     for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
     bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, scrP, scrS,
                         dq);
-    if (tab.global0) bwd_a_global<T, G>(s_off, t0, t1, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, dq);
-    if (valid && !(tab.global0 && j == 0)) {
+    if constexpr (GT) bwd_a_global<T, G>(s_off, t0, t1, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, dq);
+    if (valid && !(GT && j == 0)) {
 #pragma unroll
         for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
         S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
     }
 }
 
-template <typename T, int G, int W = kFlatWarps>
+template <typename T, int G, int W = kFlatWarps, bool GT = false>
 __global__ void __launch_bounds__(W * 32)
 bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float *scr, int bh0) {
     using S = Slice<T, G>;
@@ -755,10 +755,10 @@ bwd_flat_a_kernel(const __grid_constant__ TableArg tab, const BwdParams p, float
     grid_dep_wait();
     grid_dep_launch();
     const int r = blockIdx.y * W + (threadIdx.x >> 5);
-    if (r * R < N) bwd_flat_a_round<T, G>(tab, p, s_off, scr + (size_t)blockIdx.x * 2 * p.max_count * N, bh, r);
+    if (r * R < N) bwd_flat_a_round<T, G, GT>(tab, p, s_off, scr + (size_t)blockIdx.x * 2 * p.max_count * N, bh, r);
 }
 
-template <typename T, int G, int W = kFlatWarps>
+template <typename T, int G, int W = kFlatWarps, bool GT = false>
 __global__ void __launch_bounds__(W * 32)
 bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const float *scr, int bh0) {
     using S = Slice<T, G>;
@@ -791,8 +791,8 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
 #pragma unroll
     for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
     bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, gQ, gdelta, lg, scrP, scrS, dk, dv);
-    if (tab.global0) bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)bh * 2 * N, N, gQ, gdelta, lg, dk, dv);
-    if (valid && !(tab.global0 && k == 0)) {
+    if constexpr (GT) bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)bh * 2 * N, N, gQ, gdelta, lg, dk, dv);
+    if (valid && !(GT && k == 0)) {
 #pragma unroll
         for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
         S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
@@ -803,8 +803,8 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
 size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
 
 int g_sm_count[64] = {0};
-size_t g_fwd_smem_set[16][64] = {{0}};
-size_t g_bwd_smem_set[8][64] = {{0}};
+size_t g_fwd_smem_set[32][64] = {{0}};
+size_t g_bwd_smem_set[16][64] = {{0}};
 
 int sm_count(int dev) {
     if (dev < 0 || dev >= 64) return 148;
@@ -849,6 +849,11 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     if (const char *e = getenv("FIBATT_UNROLL")) unroll = atoi(e) == 1 ? 1 : 2;
     if (const char *e = getenv("FIBATT_FWD_THREADS")) maxt = atoi(e) == 768 ? 768 : (atoi(e) == 512 ? 512 : 1024);
     if (G == 4) maxt = 1024;
+    if (tab.global0) {   // the global-token kernels exist in the default shape only
+        G = 2;
+        unroll = 2;
+        maxt = 512;
+    }
     const int R = 32 / G;                                  // rows per warp round
     const int maxw = maxt / 32;
     // Query chunks of a multiple of R rows.  Aim for >= 8 units per SM and a
@@ -925,13 +930,13 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     return true;
 }
 
-template <typename T, int G, int UNROLL, int MAXT>
+template <typename T, int G, int UNROLL, int MAXT, bool GT = false>
 static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = fwd_pipe_kernel<T, G, UNROLL, MAXT>;
-    const int ti = (std::is_same<T, float>::value ? 0 : 8) + (G == 2 ? 0 : 4) + (UNROLL == 2 ? 0 : 2) +
-                   (MAXT == 1024 ? 0 : (MAXT == 768 ? 1 : 0));
+    auto kern = fwd_pipe_kernel<T, G, UNROLL, MAXT, GT>;
+    const int ti = (GT ? 16 : 0) + (std::is_same<T, float>::value ? 0 : 8) + (G == 2 ? 0 : 4) +
+                   (UNROLL == 2 ? 0 : 2) + (MAXT == 1024 ? 0 : (MAXT == 768 ? 1 : 0));
     if (dev >= 0 && dev < 64 && g_fwd_smem_set[ti][dev] < pl.smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
@@ -949,6 +954,8 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
 
 template <typename T>
 static cudaError_t fwd_resident_dispatch(const FwdArgs &a, const ResidentPlan &pl) {
+    if (a.tab->global0)   // the plan keeps the default shapes for it
+        return pl.lanes == 4 ? fwd_resident<T, 4, 2, 1024, true>(a, pl) : fwd_resident<T, 2, 2, 512, true>(a, pl);
     if (pl.lanes == 4) return pl.unroll == 2 ? fwd_resident<T, 4, 2, 1024>(a, pl) : fwd_resident<T, 4, 1, 1024>(a, pl);
     if (pl.maxt == 768) return pl.unroll == 2 ? fwd_resident<T, 2, 2, 768>(a, pl) : fwd_resident<T, 2, 1, 768>(a, pl);
     return pl.unroll == 2 ? fwd_resident<T, 2, 2, 512>(a, pl) : fwd_resident<T, 2, 1, 512>(a, pl);
@@ -968,11 +975,11 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     // work than four; measured faster), four for fp32 rows (two would spill)
     int G = dt == FIBATT_F32 ? 4 : 2;
     if (const char *e = getenv("FIBATT_BWD_LANES")) G = atoi(e) == 2 ? 2 : 4;
-    if (dt == FIBATT_F32) G = 4;
+    if (dt == FIBATT_F32 || tab.global0) G = dt == FIBATT_F32 ? 4 : 2;   // global token: default shape only
     const int R = 32 / G;
     int maxt = 512;
     if (const char *e = getenv("FIBATT_BWD_THREADS")) maxt = atoi(e) == 1024 ? 1024 : 512;
-    if (G == 2) maxt = 512;
+    if (G == 2 || tab.global0) maxt = 512;
     const int maxw = maxt / 32;
     const size_t stage = (4 * (size_t)N * RB + 2 * (size_t)N * sizeof(float) + 127) / 128 * 128;
     const size_t scratch = (2 * (size_t)std::max(1, tab.max_count) * N * 4 + 127) / 128 * 128;
@@ -1005,9 +1012,11 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     int dev = 0;
     cudaGetDevice(&dev);
     const int ti = std::is_same<T, float>::value ? 0 : 1;
-    auto kern = pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512>
-                              : (pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>);
-    const int ki = ti * 4 + (pl.lanes == 2 ? 2 : (pl.threads > 512 ? 1 : 0));
+    const bool gt = a.tab->global0 != 0;
+    auto kern = gt ? (pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512, true> : bwd_pipe_kernel<T, 4, 512, true>)
+            : pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512>
+                            : (pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>);
+    const int ki = ti * 8 + (gt ? 4 : 0) + (pl.lanes == 2 ? 2 : (pl.threads > 512 ? 1 : 0));
     if (dev >= 0 && dev < 64 && g_bwd_smem_set[ki][dev] < pl.smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e != cudaSuccess) return e;
@@ -1023,7 +1032,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
 }
 
 // Units [bh0, bh0 + count); the scratch a.Dws holds `count` units' weights.
-template <typename T, int G, int W = kFlatWarps>
+template <typename T, int G, int W = kFlatWarps, bool GT = false>
 static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
@@ -1033,10 +1042,10 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     const bool pdl = pdl_enabled();
     float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N
     cudaError_t e =
-        launch_kernel(bwd_flat_a_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p, scr, bh0);
+        launch_kernel(bwd_flat_a_kernel<T, G, W, GT>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p, scr, bh0);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_kernel(bwd_flat_b_kernel<T, G, W>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p,
+    e = launch_kernel(bwd_flat_b_kernel<T, G, W, GT>, grid, dim3(W * 32), 0, a.stream, pdl, tab, p,
                       static_cast<const float *>(scr), bh0);
     count_launches(2);
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -1046,6 +1055,9 @@ cudaError_t launch_bwd_flat(const BwdArgs &a) {
     int G = 4;
     if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
     const int units = a.B * a.tab->H;
+    if (a.tab->global0)
+        return a.dtype == FIBATT_F32 ? bwd_flat<float, 4, kFlatWarps, true>(a, 0, units)
+                                     : bwd_flat<__nv_bfloat16, 4, kFlatWarps, true>(a, 0, units);
     if (a.dtype == FIBATT_F32) return bwd_flat<float, 4>(a, 0, units);
     return G == 2 ? bwd_flat<__nv_bfloat16, 2>(a, 0, units) : bwd_flat<__nv_bfloat16, 4>(a, 0, units);
 }
@@ -1059,7 +1071,7 @@ cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
     return a.dtype == FIBATT_F32 ? bwd_resident<float>(a, pl, units) : bwd_resident<__nv_bfloat16>(a, pl, units);
 }
 
-template <typename T, int G, int W = kFlatWarps, int U = 2>
+template <typename T, int G, int W = kFlatWarps, int U = 2, bool GT = false>
 static cudaError_t fwd_flat(const FwdArgs &a) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
@@ -1071,7 +1083,7 @@ static cudaError_t fwd_flat(const FwdArgs &a) {
     p.LSE = a.LSE;
     p.scale_log2 = a.scale * kLog2e;
     const dim3 grid((unsigned)(a.B * tab.H), (unsigned)((tab.N + R * W - 1) / (R * W)));
-    const cudaError_t e = launch_kernel(fwd_flat_kernel<T, G, U, W>, grid, dim3(W * 32), 0, a.stream,
+    const cudaError_t e = launch_kernel(fwd_flat_kernel<T, G, U, W, GT>, grid, dim3(W * 32), 0, a.stream,
                                         pdl_enabled(), tab, p);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -1080,6 +1092,9 @@ static cudaError_t fwd_flat(const FwdArgs &a) {
 cudaError_t launch_fwd_flat(const FwdArgs &a) {
     int G = 4;   // four lanes per row: more warps in flight to cover global-load latency (measured faster)
     if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
+    if (a.tab->global0)
+        return a.dtype == FIBATT_F32 ? fwd_flat<float, 4, kFlatWarps, 2, true>(a)
+                                     : fwd_flat<__nv_bfloat16, 4, kFlatWarps, 2, true>(a);
     if (a.dtype == FIBATT_F32) return G == 4 ? fwd_flat<float, 4>(a) : fwd_flat<float, 2>(a);
     return G == 4 ? fwd_flat<__nv_bfloat16, 4>(a) : fwd_flat<__nv_bfloat16, 2>(a);
 }
