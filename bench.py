@@ -54,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="vitb")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--block", action="store_true",
+                   help="time the attention layer (QKV projection, Fibottention, output projection) fwd+bwd "
+                        "instead of the attention core, next to the same layer with masked dense attention")
     p.add_argument("--global-token", action="store_true",
                    help="token 0 global in every head (README Algorithm 2's class token)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -511,10 +514,64 @@ def reference_arm(args):
     print(json.dumps(out), flush=True)
 
 
+def block_arm(args):
+    """The attention layer of a ViT block (sparse_head_self_gb300.block) as a
+    training step: forward and backward through autograd, synthetic input of
+    the workload's shape, dim = H * 64; next to it the same layer with its
+    attention core written as torch scaled-dot-product attention under the
+    support's boolean mask (dense work, same result)."""
+    from sparse_head_self_gb300.block import FibottentionSelfAttention
+    import oracle
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.manual_seed(0)
+    layer = FibottentionSelfAttention(wl.H * 64, wl.H, wl.N, wl.w_min, wl.w_max, wl.diag,
+                                      global_token=args.global_token).to(dev, wl.torch_dtype)
+    x = torch.randn(wl.B, wl.N, wl.H * 64, device=dev, dtype=wl.torch_dtype, requires_grad=True)
+    g = torch.randn_like(x)
+    heads = _oracle_heads(wl, args.global_token)
+    mask = torch.stack([torch.from_numpy(oracle.support_mask(wl.N, h).astype(bool)) for h in heads]).to(dev)
+
+    def dense_layer(xx):
+        B, N, dim = xx.shape
+        qkv = layer.qkv(xx).view(B, N, 3, wl.H, 64).permute(2, 0, 3, 1, 4)
+        o = torch.nn.functional.scaled_dot_product_attention(qkv[0], qkv[1], qkv[2], attn_mask=mask[None],
+                                                             scale=layer.scale)
+        return layer.proj(o.transpose(1, 2).reshape(B, N, dim))
+
+    def time_steps(fn, n):
+        for _ in range(max(3, args.warmup)):
+            fn(x).backward(g)
+        torch.cuda.synchronize(dev)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(n):
+            fn(x).backward(g)
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / n
+
+    K = min(args.steps, 500)
+    ms = time_steps(layer, K)
+    ms_dense = time_steps(dense_layer, K)
+    tokens = wl.B * wl.N
+    out = {"metric": "attention layer training step (QKV projection, attention, output projection; fwd+bwd)",
+           "value": tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": max(3, args.warmup),
+           "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": wl.dtype, "data": "synthetic",
+           "config": {"workload": f"{wl.name}: B={wl.B} N={wl.N} dim={wl.H * 64} heads={wl.H}"
+                                  + (", global token 0" if args.global_token else ""),
+                      "layer": "Linear(dim, 3 dim) -> Fibottention -> Linear(dim, dim)"},
+           "dense_masked_sdpa": {"ms_per_step": ms_dense, "tokens_per_s": tokens / (ms_dense / 1e3)}}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         reference_arm(args)
+    elif args.block:
+        block_arm(args)
     else:
         gb300_arm(args)
 
