@@ -63,6 +63,7 @@ struct PipeParams {
     int n_keep;
     int qsub;
     int sub_rows;
+    int early_prefetch;   // L2-prefetch the first units before the grid-dependency wait
 };
 
 struct Unit {
@@ -287,6 +288,16 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     __shared__ int s_off[kMaxEntries];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0 && p.early_prefetch) {
+        // Warm L2 with the first units' rows while the previous kernel drains.
+        // A prefetch only moves lines into L2, the point of coherence: the
+        // copies issued after the grid-dependency wait below still read what
+        // the previous kernel wrote.
+        for (int i = 0; i < p.stages; ++i) {
+            const int u = (int)blockIdx.x + i * (int)gridDim.x;
+            if (u < p.n_units) prefetch_unit<T>(tab, p, u);
+        }
+    }
     for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -466,6 +477,7 @@ struct BwdParams {
     uint32_t scratch_off;   // byte offset of the P/dS scratch in dynamic smem
     int max_count;          // max table entries of one head (scratch rows)
     const float *gw;        // global first token: P_0k, dS_0k ([B*H][2][N]), or NULL
+    int early_prefetch;     // L2-prefetch the first units before the grid-dependency wait
 };
 
 // Phase A for one round of query rows, branch-free: the key row is clamped
@@ -570,6 +582,19 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 
     const int N = tab.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0 && p.early_prefetch) {
+        // as in the forward: warm L2 with the first units' rows early
+        const uint32_t b = (uint32_t)((size_t)N * RB);
+        for (int i = 0; i < p.stages; ++i) {
+            const int u = (int)blockIdx.x + i * (int)gridDim.x;
+            if (u >= p.n_units) break;
+            const size_t row0 = (size_t)u * N * kHeadDim;
+            bulk_prefetch_l2(static_cast<const T *>(p.Q) + row0, b);
+            bulk_prefetch_l2(static_cast<const T *>(p.K) + row0, b);
+            bulk_prefetch_l2(static_cast<const T *>(p.V) + row0, b);
+            bulk_prefetch_l2(static_cast<const T *>(p.dO) + row0, b);
+        }
+    }
     for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -802,6 +827,16 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
 
 size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
 
+// Early L2 prefetch of each CTA's first units (FIBATT_EARLY_PREFETCH=0 turns
+// it off); it only pays with dependent launches.
+int early_prefetch() {
+    static const int on = [] {
+        const char *e = getenv("FIBATT_EARLY_PREFETCH");
+        return (e && atoi(e) == 0) ? 0 : 1;
+    }();
+    return on && pdl_enabled();
+}
+
 int g_sm_count[64] = {0};
 size_t g_fwd_smem_set[32][64] = {{0}};
 size_t g_bwd_smem_set[16][64] = {{0}};
@@ -945,7 +980,7 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     const int n_reg = a.B * a.tab->H * pl.qsplit;
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
                  pl.n_keep + (n_reg - pl.n_keep) * pl.qsub, pl.stages, pl.groups, pl.gwarps,
-                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows};
+                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows, early_prefetch()};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -1024,7 +1059,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     }
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 units, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
-                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw};
+                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch()};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -1037,7 +1072,7 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw};
+                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0};
     const dim3 grid((unsigned)count, (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
     float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N
