@@ -282,35 +282,68 @@ class Step:
 
 def run_e2e(step: Step, dev, steps: int):
     """Same step through the public Python API, with the inputs copied from
-    pinned host memory and every output read back to pinned host memory."""
+    pinned host memory and every output read back to pinned host memory.
+
+    Steps are pipelined two deep: step i's host-to-device copies (copy
+    stream), fwd + bwd (compute stream) and device-to-host copies (second
+    copy stream) overlap with those of steps i - 1 and i + 1, on two device
+    buffer sets; events keep every buffer from being overwritten before its
+    last reader is done."""
     wl = step.wl
     q, k, v, do = (x.pin_memory() for x in step.host)
-    outs = {n: torch.empty((wl.B, wl.H, wl.N, wl.D), dtype=wl.torch_dtype).pin_memory()
-            for n in ("O", "dQ", "dK", "dV")}
-    outs["LSE"] = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
-    t = step.sets[0]
+    out_sets = []
+    for _ in range(2):
+        outs = {n: torch.empty((wl.B, wl.H, wl.N, wl.D), dtype=wl.torch_dtype).pin_memory()
+                for n in ("O", "dQ", "dK", "dV")}
+        outs["LSE"] = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
+        out_sets.append(outs)
+    sets = step.sets[:2]
     h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do))
-    d2h = sum(x.numel() * x.element_size() for x in outs.values())
+    d2h = sum(x.numel() * x.element_size() for x in out_sets[0].values())
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def one():
+    def one(i):
+        c = i % 2
+        t, outs = sets[c], out_sets[c]
         sup = api.Support.wythoff(wl.H, wl.N, wl.w_min, wl.w_max, wl.diag).set_global_token(step.global_token)
-        for n, x in zip(("Q", "K", "V", "dO"), (q, k, v, do)):
-            t[n].copy_(x, non_blocking=True)
-        api.fwd(sup, t["Q"], t["K"], t["V"], wl.scale, O=t["O"], LSE=t["LSE"])
-        api.bwd(sup, t["Q"], t["K"], t["V"], t["O"], t["LSE"], t["dO"], wl.scale, dQ=t["dQ"],
-                dK=t["dK"], dV=t["dV"], workspace=t["ws"])
-        for n in ("O", "LSE", "dQ", "dK", "dV"):
-            outs[n].copy_(t[n], non_blocking=True)
+        with torch.cuda.stream(s_in):
+            if used[c]:
+                s_in.wait_event(ev_cmp[c])      # step i-2 done reading these inputs
+            for n, x in zip(("Q", "K", "V", "dO"), (q, k, v, do)):
+                t[n].copy_(x, non_blocking=True)
+            ev_in[c].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[c])
+            if used[c]:
+                s_cmp.wait_event(ev_out[c])     # step i-2's outputs read back
+            api.fwd(sup, t["Q"], t["K"], t["V"], wl.scale, O=t["O"], LSE=t["LSE"], stream=s_cmp)
+            api.bwd(sup, t["Q"], t["K"], t["V"], t["O"], t["LSE"], t["dO"], wl.scale, dQ=t["dQ"],
+                    dK=t["dK"], dV=t["dV"], workspace=t["ws"], stream=s_cmp)
+            ev_cmp[c].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[c])
+            for n in ("O", "LSE", "dQ", "dK", "dV"):
+                outs[n].copy_(t[n], non_blocking=True)
+            ev_out[c].record(s_out)
+        used[c] = True
         sup.close()
 
-    for _ in range(3):
-        one()
+    for i in range(4):
+        one(i)
     torch.cuda.synchronize(dev)
+    main = torch.cuda.current_stream(dev)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        one()
-    e.record()
+    s.record(main)
+    s_in.wait_stream(main)
+    for i in range(steps):
+        one(i)
+    main.wait_stream(s_out)
+    main.wait_stream(s_cmp)
+    e.record(main)
     torch.cuda.synchronize(dev)
     ms = s.elapsed_time(e) / steps
     return ms, h2d, d2h
