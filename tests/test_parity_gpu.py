@@ -134,6 +134,27 @@ def test_resident_last_wave_pieces(split, monkeypatch):
 
 
 @pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
+@pytest.mark.parametrize("scale", [0.0, 1e-3, -0.5, 3.0])
+def test_extreme_scales(scale, kernel_path):
+    # uniform weights (scale 0), nearly uniform, negative, and peaked
+    # softmaxes (the running maximum is raised many times) in fp32
+    wl = Workload(**{**WORKLOADS["vitb"].__dict__, "B": 1, "dtype": "f32", "scale": scale})
+    q, k, v, do = make_inputs(wl, 31)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, scale)
+    heads = oracle_heads(wl)
+    O_r, L_r = oracle.fwd(q, k, v, heads, scale)
+    rQ, rK, rV = oracle.bwd(q, k, v, do, heads, scale)
+    # the peaked case has scores up to ~40 (natural units): compare relative to the magnitudes
+    tol = 1e-5 * max(1.0, abs(scale) * 8)
+    for n, g, r in (("O", O, O_r), ("LSE", L, L_r), ("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV)):
+        d = np.abs(g.double().cpu().numpy() - r)
+        assert d.max() <= tol * max(1.0, float(np.abs(r).max())), f"{n} scale {scale}: {d.max():.3e}"
+
+
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 def test_empty_support_rows_are_zero(kernel_path):
     # N = 3, row 2 of the Wythoff array (4, 7), no diagonal: no pair at all
     N = 3
@@ -312,6 +333,43 @@ def test_global_token_only_support_gives_v0():
     O, L = api.fwd(sup, *to_dev(q, k, v), wl.scale)
     torch.cuda.synchronize()
     assert torch.equal(O[:, :, 1:].cpu(), v[:, :, :1].expand(B, 2, N - 1, 64))
+
+
+@pytest.mark.parametrize("name", ["vitb", "video"])
+def test_cuda_graph_capture_replays_the_step(name):
+    # the support travels as a kernel argument and the calls neither allocate
+    # nor synchronise, so fwd + bwd can be captured once and replayed; the
+    # first (eager) call sets up the plans before the capture
+    wl = WORKLOADS[name].with_batch(2)
+    sup = support_for(wl)
+    q, k, v, do = make_inputs(wl, 41)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O = torch.empty_like(qd)
+    L = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device="cuda")
+    dQ, dK, dV = (torch.empty_like(qd) for _ in range(3))
+    ws = torch.empty(sup.bwd_workspace_bytes(wl.B), dtype=torch.uint8, device="cuda")
+
+    def step():
+        api.fwd(sup, qd, kd, vd, wl.scale, O=O, LSE=L)
+        api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (O, L, dQ, dK, dV)]
+    g = torch.cuda.CUDAGraph()
+    for t in (O, L, dQ, dK, dV):
+        t.zero_()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip((O, L, dQ, dK, dV), ref):
+        assert torch.equal(a, b)
 
 
 # ----------------------------------------------- full sizes, bench launches
