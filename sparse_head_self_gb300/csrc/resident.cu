@@ -625,6 +625,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
                 bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
                 bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
+                if (i == 0) {   // the consumers compute the first unit's D_j from these
+                    bulk_prefetch_l2(static_cast<const T *>(p.O) + row0 * kHeadDim, b);
+                    if ((N * 4) % 16 == 0 && (row0 * 4) % 16 == 0) bulk_prefetch_l2(p.LSE + row0, (uint32_t)N * 4);
+                }
                 const int un = u + gridDim.x;
                 if (un < p.n_units) {
                     bulk_prefetch_l2(static_cast<const T *>(p.O) + (size_t)un * N * kHeadDim, b);
@@ -633,6 +637,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 }
             }
             __syncwarp();
+            if (i == 0) {   // first unit: the consumers, idle until its rows land, fill D_j and LSE_j
+                if (lane == 0) mbar_arrive(&aux_bar[s]);
+                continue;
+            }
             if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
             float *sD = reinterpret_cast<float *>(st + 4 * tens), *sL = sD + N;
             for (int j = lane; j < N; j += 32) {
@@ -663,6 +671,18 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         const int h = u % tab.H;
         const int t0 = tab.start[h], t1 = tab.start[h + 1];
         const size_t row0 = (size_t)u * N;
+        if (i == 0) {
+            // the first unit's D_j = <dO_j, O_j> and LSE_j (log2 units), one
+            // row per consumer thread: the producer warp would take all the
+            // rows' global-load round trips in turn while every consumer waits
+            float *wD = reinterpret_cast<float *>(smem + (size_t)s * p.stage_bytes + 4 * tens), *wL = wD + N;
+            for (int j = cw * 32 + lane; j < N; j += cthreads) {
+                wD[j] = row_dot_global_shared(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim,
+                                              st + 3 * tens + (size_t)j * RB, lane);
+                wL[j] = p.LSE[row0 + j] * kLog2e;
+            }
+            consumer_sync(cthreads);
+        }
         // ---- phase A: query rows
         for (int r = cw; r < nrounds; r += p.cwarps) {
             const int jl = r * R + lane / G;
@@ -1048,9 +1068,14 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     cudaGetDevice(&dev);
     const int ti = std::is_same<T, float>::value ? 0 : 1;
     const bool gt = a.tab->global0 != 0;
-    auto kern = gt ? (pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512, true> : bwd_pipe_kernel<T, 4, 512, true>)
-            : pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512>
-                            : (pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>);
+    decltype(&bwd_pipe_kernel<T, 4, 512>) kern;
+    if constexpr (std::is_same<T, float>::value)   // fp32 rows: four lanes per row only
+        kern = gt ? bwd_pipe_kernel<T, 4, 512, true>
+                  : (pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>);
+    else
+        kern = gt ? (pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512, true> : bwd_pipe_kernel<T, 4, 512, true>)
+                  : pl.lanes == 2 ? bwd_pipe_kernel<T, 2, 512>
+                                  : (pl.threads > 512 ? bwd_pipe_kernel<T, 4, 1024> : bwd_pipe_kernel<T, 4, 512>);
     const int ki = ti * 8 + (gt ? 4 : 0) + (pl.lanes == 2 ? 2 : (pl.threads > 512 ? 1 : 0));
     if (dev >= 0 && dev < 64 && g_bwd_smem_set[ki][dev] < pl.smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
