@@ -95,10 +95,14 @@ __device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const PipePar
     return g;
 }
 
+// Running state of one query row: acc = sum of weight x value row, m the
+// running maximum (log2 units), l the sum of the weights (for the LSE) and
+// lt the sum of the weights as they entered acc (rounded to bf16 when the
+// P.V update takes bf16 weights), which normalises O.
 template <int G>
 struct SoftmaxState {
     float2 acc[32 / G];
-    float m, l;
+    float m, l, lt;
 };
 
 template <int G>
@@ -106,6 +110,7 @@ __device__ __forceinline__ void softmax_raise(SoftmaxState<G> &st, float s) {
     if (s > st.m + 8.f) {
         const float a = fast_exp2(st.m - s);
         st.l *= a;
+        st.lt *= a;
 #pragma unroll
         for (int i = 0; i < 32 / G; ++i) st.acc[i] = mul2(st.acc[i], make_float2(a, a));
         st.m = s;
@@ -129,12 +134,38 @@ struct LaneGeom {
 // 2^(-inf - m) = 0 instead of a NaN, and any real score raises it.
 constexpr float kMaxInit = -1.0e30f;
 
+// Weight p of value row vr into the state.  W16 (bf16 rows): p is rounded
+// to bf16 for the row update, as bf16 attention kernels round P before their
+// P.V product, which makes the update one mixed-precision FMA per element;
+// O is normalised by the sum of the rounded weights, so it stays a convex
+// combination of the value rows and the largest weight's rounding cancels.
+template <typename T, int G, bool W16>
+__device__ __forceinline__ void softmax_accumulate(SoftmaxState<G> &st, const Slice<T, G> &vr, float p) {
+    st.l += p;
+    if constexpr (W16 && std::is_same<T, __nv_bfloat16>::value) {
+        const uint32_t p2 = bf16x2_splat(p);
+        st.lt += __uint_as_float(p2 << 16);
+        vr.axpy_p2(p2, st.acc);
+    } else {
+        vr.axpy(p, st.acc);   // lt is l here (softmax_norm reads l)
+    }
+}
+
+// The sum that normalises O (see softmax_accumulate).
+template <typename T, int G, bool W16>
+__device__ __forceinline__ float softmax_norm(const SoftmaxState<G> &st) {
+    if constexpr (W16 && std::is_same<T, __nv_bfloat16>::value) return st.lt;
+    else return st.l;
+}
+
 // One pass over offsets [tb, te) (read from the shared-memory copy `off`) for
 // query row j, branch-free: the key row is clamped into the staged window
 // [lo, lo + nrows) and a score whose key lies outside [0, N) (or whose row is
 // padding) becomes -inf, so its weight is exactly 0 and the raise never
 // triggers.  Two offsets per step so their shared-memory loads overlap.
-template <typename T, int G, int UNROLL>
+// W16: bf16 weights in the P.V update (softmax_accumulate; the
+// shared-memory kernels, where it saves issue slots), else fp32 weights.
+template <typename T, int G, int UNROLL, bool W16>
 __device__ __forceinline__ void fwd_offsets(const int *off, int N, int tb, int te, int j, bool valid, int lo,
                                             int nrows, const uint8_t *sK, ptrdiff_t vdelta, const Slice<T, G> &q,
                                             const LaneGeom<T, G> &lg, float sl2, SoftmaxState<G> &st) {
@@ -157,11 +188,10 @@ __device__ __forceinline__ void fwd_offsets(const int *off, int N, int tb, int t
             s1 = in1 ? s1 : -INFINITY;
             softmax_raise(st, fmaxf(s0, s1));
             const float p0 = fast_exp2(s0 - st.m), p1 = fast_exp2(s1 - st.m);
-            st.l += p0 + p1;
             k0r.load(a0 + vdelta, lg.c);
             k1r.load(a1 + vdelta, lg.c);
-            k0r.axpy(p0, st.acc);
-            k1r.axpy(p1, st.acc);
+            softmax_accumulate<T, G, W16>(st, k0r, p0);
+            softmax_accumulate<T, G, W16>(st, k1r, p1);
         }
     }
     for (; t < te; ++t) {
@@ -174,9 +204,8 @@ __device__ __forceinline__ void fwd_offsets(const int *off, int N, int tb, int t
         s = in ? s : -INFINITY;
         softmax_raise(st, s);
         const float pr = fast_exp2(s - st.m);
-        st.l += pr;
         kv.load(a + vdelta, lg.c);
-        kv.axpy(pr, st.acc);
+        softmax_accumulate<T, G, W16>(st, kv, pr);
     }
 }
 
@@ -210,7 +239,7 @@ __device__ __forceinline__ bool table_has(const int *off, int t0, int t1, int v)
 }
 
 // Round r of a unit: query rows [q0 + r R, q0 + r R + R) with R = 32 / G.
-template <typename T, int G, int UNROLL, bool GT = false>
+template <typename T, int G, int UNROLL, bool GT, bool W16>
 __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, const PipeParams &p, const Unit &g,
                                           const uint8_t *sQ, const uint8_t *sK, ptrdiff_t vdelta, int r,
                                           const LaneGeom<T, G> &lg, const uint8_t *sK0 = nullptr,
@@ -239,7 +268,8 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
     for (int i = 0; i < 32 / G; ++i) st.acc[i] = make_float2(0.f, 0.f);
     st.m = kMaxInit;
     st.l = 0.f;
-    fwd_offsets<T, G, UNROLL>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
+    st.lt = 0.f;
+    fwd_offsets<T, G, UNROLL, W16>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
     if constexpr (GT) {
         // global first token: key 0 for every query row j >= 1 whose band
         // misses it (offset -j absent; the tables are symmetric)
@@ -250,12 +280,12 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
         s0 = need ? s0 : -INFINITY;
         softmax_raise(st, s0);
         const float pr = fast_exp2(s0 - st.m);
-        st.l += pr;
         kr.load(sV0, lg.c);
-        kr.axpy(pr, st.acc);
+        softmax_accumulate<T, G, W16>(st, kr, pr);
     }
     if (valid) {
-        const float inv = st.l > 0.f ? __frcp_rn(st.l) : 0.f;
+        const float ln = softmax_norm<T, G, W16>(st);
+        const float inv = ln > 0.f ? __frcp_rn(ln) : 0.f;
 #pragma unroll
         for (int i = 0; i < 32 / G; ++i) st.acc[i] = mul2(st.acc[i], make_float2(inv, inv));
         S::store(gO + (size_t)j * kHeadDim, lg.c, st.acc);
@@ -369,7 +399,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const Unit g = unit_geometry(tab, p, u);
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         for (int r = wg; r < rpu; r += p.gwarps)
-            fwd_round<T, G, UNROLL, GT>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
+            fwd_round<T, G, UNROLL, GT, true>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
                                     st + g0_off, st + g0_off + RB);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -412,7 +442,7 @@ fwd_flat_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
     const LaneGeom<T, G> lg;
     const int r = blockIdx.y * W + (threadIdx.x >> 5);
-    fwd_round<T, G, UNROLL, GT>(tab, s_off, p, g, gQ, gK, vdelta, r, lg, gK, gK + vdelta);
+    fwd_round<T, G, UNROLL, GT, false>(tab, s_off, p, g, gQ, gK, vdelta, r, lg, gK, gK + vdelta);
 }
 
 // ---------------------------------------------------------------- backward

@@ -111,6 +111,27 @@ __device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
 // (c.x + a.x*b.x, c.y + a.y*b.y), each an IEEE fma (packed f32x2, sm_100+).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
+// (c.x, c.y) + (lo(w), hi(w)) * (lo(p2), hi(p2)) for packed bf16 pairs w and
+// p2, products exact and accumulated in fp32 (one mixed-precision FMA per
+// element, no unpacking of w).
+__device__ __forceinline__ float2 fma2_bf16(uint32_t p2, uint32_t w, float2 c) {
+    asm("{\n\t.reg .b16 pl, ph, wl, wh;\n\t"
+        "mov.b32 {pl, ph}, %2;\n\t"
+        "mov.b32 {wl, wh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, pl, wl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, ph, wh, %1;\n\t}"
+        : "+f"(c.x), "+f"(c.y)
+        : "r"(p2), "r"(w));
+    return c;
+}
+
+// p rounded to bf16 (nearest even) in both halves of a packed pair.
+__device__ __forceinline__ uint32_t bf16x2_splat(float p) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(p));
+    return r;
+}
+
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // 2^x on the SFU (ex2.approx.ftz, relative error about 2^-22; results below
@@ -170,7 +191,7 @@ struct SliceBf16 {
         }
         return (a + b) + (c + d);
     }
-    // acc[4i + e] += p * (element pair e of chunk i)
+    // acc[4i + e] += p * (element pair e of chunk i), fp32 weight
     __device__ __forceinline__ void axpy(float p, float2 (&acc)[kPairs]) const {
         const float2 pp = make_float2(p, p);
 #pragma unroll
@@ -179,6 +200,19 @@ struct SliceBf16 {
             acc[4 * i + 1] = fma2(pp, make_float2(bf16_lo(w[i].y), bf16_hi(w[i].y)), acc[4 * i + 1]);
             acc[4 * i + 2] = fma2(pp, make_float2(bf16_lo(w[i].z), bf16_hi(w[i].z)), acc[4 * i + 2]);
             acc[4 * i + 3] = fma2(pp, make_float2(bf16_lo(w[i].w), bf16_hi(w[i].w)), acc[4 * i + 3]);
+        }
+    }
+    // The same update with a weight already rounded to bf16 (p2: both halves
+    // of a packed pair, from bf16x2_splat): one mixed-precision FMA per
+    // element (exact product, fp32 sum) instead of an unpack and half a
+    // packed FMA.
+    __device__ __forceinline__ void axpy_p2(uint32_t p2, float2 (&acc)[kPairs]) const {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            acc[4 * i + 0] = fma2_bf16(p2, w[i].x, acc[4 * i + 0]);
+            acc[4 * i + 1] = fma2_bf16(p2, w[i].y, acc[4 * i + 1]);
+            acc[4 * i + 2] = fma2_bf16(p2, w[i].z, acc[4 * i + 2]);
+            acc[4 * i + 3] = fma2_bf16(p2, w[i].w, acc[4 * i + 3]);
         }
     }
     // store acc (in this lane's chunk order) to a global row, RNE to bf16
