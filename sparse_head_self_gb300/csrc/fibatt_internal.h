@@ -91,9 +91,10 @@ struct ResidentPlan {
     int groups;          // consumer warp groups
     int gwarps;          // warps per consumer group
     int prefetch;        // units beyond the ring warmed in L2 (forward)
-    int n_keep;          // forward: whole units before the last partial wave
-    int qsub;            // forward: pieces each last-wave unit is cut into
-    int sub_rows;        // forward: query rows per piece
+    int n_keep;          // whole units before the last partial wave
+    int qsub;            // pieces each last-wave unit is cut into
+    int sub_rows;        // forward: query rows per piece; backward: rounds per piece
+    size_t split_off;    // backward: byte offset of the pieces' (P, dS) areas
     size_t stage_bytes;  // bytes per ring stage
     size_t smem;         // dynamic shared memory bytes
     int threads;         // threads per CTA (producer warp + consumers)

@@ -508,7 +508,67 @@ struct BwdParams {
     int max_count;          // max table entries of one head (scratch rows)
     const float *gw;        // global first token: P_0k, dS_0k ([B*H][2][N]), or NULL
     int early_prefetch;     // L2-prefetch the first units before the grid-dependency wait
+    // Items: [0, n_keep) are whole units; then the units n_keep, n_keep + 1,
+    // ... (the partial last wave) as `pieces` pieces each, piece q holding
+    // rounds [q piece_rounds, (q + 1) piece_rounds) of both phases, with P and
+    // dS recomputed in phase B so a piece needs no other piece's scratch.
+    // n_units counts items.
+    int n_keep;
+    int pieces;
+    int piece_rounds;
+    uint32_t piece_off;   // per phase-B warp of a piece: [max_count][R] (P, dS) pairs
 };
+
+__device__ __forceinline__ int bwd_item_unit(const BwdParams &p, int u) {
+    return u < p.n_keep ? u : p.n_keep + (u - p.n_keep) / p.pieces;
+}
+
+// Phase B for one round of key rows with P and dS recomputed from the staged
+// rows (pieces of a split unit), in two passes that keep the register count
+// of the two-phase path: first s = <q_j, k>, dP = <dO_j, v>, P from the row's
+// LSE and dS = P (dP - D_j) for every offset into this warp's area pw
+// ([te - tb][R] pairs of P, dS), then the row updates as in bwd_b_offsets.
+template <typename T, int G>
+__device__ __forceinline__ void bwd_b_recompute_offsets(const int *off, int N, int tb, int te, int k, bool valid,
+                                                        const uint8_t *sQ, const uint8_t *sK, ptrdiff_t tens,
+                                                        const float *sD, const float *sL, float sl2,
+                                                        const LaneGeom<T, G> &lg, float2 *pw,
+                                                        float2 (&dk)[32 / G], float2 (&dv)[32 / G]) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
+    const int lane = threadIdx.x & 31, row = lane / G;
+    const bool writer = (lane & (G - 1)) == 0;
+    {
+        S kk, vv;
+        kk.load(sK + (ptrdiff_t)k * RB, lg.c);
+        vv.load(sK + tens + (ptrdiff_t)k * RB, lg.c);
+        for (int t = tb; t < te; ++t) {
+            const int j = k + off[t];
+            const bool in = valid && j >= 0 && j < N;
+            const int jc = min(max(j, 0), N - 1);
+            const uint8_t *a = sQ + (ptrdiff_t)jc * RB;
+            S qq, gg;
+            qq.load(a, lg.c);
+            gg.load(a + 3 * tens, lg.c);
+            const float sc = group_sum<G>(qq.dot(kk));
+            const float dp = group_sum<G>(gg.dot(vv));
+            const float P = in ? fast_exp2(fmaf(sc, sl2, -sL[jc])) : 0.f;
+            if (writer) pw[(t - tb) * R + row] = make_float2(P, P * (dp - sD[jc]));
+        }
+    }
+    __syncwarp();
+    for (int t = tb; t < te; ++t) {
+        const int jc = min(max(k + off[t], 0), N - 1);
+        const float2 w = pw[(t - tb) * R + row];
+        const uint8_t *a = sQ + (ptrdiff_t)jc * RB;
+        S qq, gg;
+        qq.load(a, lg.c);
+        gg.load(a + 3 * tens, lg.c);
+        qq.axpy(w.y, dk);
+        gg.axpy(w.x, dv);
+    }
+}
 
 // Phase A for one round of query rows, branch-free: the key row is clamped
 // into [0, N) and an out-of-range pair gets P = 0 (so dS = 0 too); only
@@ -616,9 +676,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         // as in the forward: warm L2 with the first units' rows early
         const uint32_t b = (uint32_t)((size_t)N * RB);
         for (int i = 0; i < p.stages; ++i) {
-            const int u = (int)blockIdx.x + i * (int)gridDim.x;
-            if (u >= p.n_units) break;
-            const size_t row0 = (size_t)u * N * kHeadDim;
+            const int it = (int)blockIdx.x + i * (int)gridDim.x;
+            if (it >= p.n_units) break;
+            const size_t row0 = (size_t)bwd_item_unit(p, it) * N * kHeadDim;
             bulk_prefetch_l2(static_cast<const T *>(p.Q) + row0, b);
             bulk_prefetch_l2(static_cast<const T *>(p.K) + row0, b);
             bulk_prefetch_l2(static_cast<const T *>(p.V) + row0, b);
@@ -643,11 +703,12 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         // from global memory, prefetched into L2 a unit ahead) and LSE_j in
         // log2 units, so no consumer waits on a global load
         int i = 0;
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+        for (int it = blockIdx.x; it < p.n_units; it += gridDim.x, ++i) {
             const int s = i % p.stages;
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
-            const size_t row0 = (size_t)u * N;
+            const bool fill_by_consumers = i == 0 || (!GT && it >= p.n_keep);
+            const size_t row0 = (size_t)bwd_item_unit(p, it) * N;
             if (lane == 0) {
                 const uint32_t b = (uint32_t)tens;
                 mbar_expect_tx(&full_bar[s], 4 * b);
@@ -655,19 +716,23 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
                 bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
                 bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
-                if (i == 0) {   // the consumers compute the first unit's D_j from these
+                if (fill_by_consumers) {   // the consumers compute these D_j
                     bulk_prefetch_l2(static_cast<const T *>(p.O) + row0 * kHeadDim, b);
                     if ((N * 4) % 16 == 0 && (row0 * 4) % 16 == 0) bulk_prefetch_l2(p.LSE + row0, (uint32_t)N * 4);
                 }
-                const int un = u + gridDim.x;
-                if (un < p.n_units) {
+                const int itn = it + gridDim.x;
+                if (itn < p.n_units) {
+                    const int un = bwd_item_unit(p, itn);
                     bulk_prefetch_l2(static_cast<const T *>(p.O) + (size_t)un * N * kHeadDim, b);
                     if ((N * 4) % 16 == 0 && ((size_t)un * N * 4) % 16 == 0)
                         bulk_prefetch_l2(p.LSE + (size_t)un * N, (uint32_t)N * 4);
                 }
             }
             __syncwarp();
-            if (i == 0) {   // first unit: the consumers, idle until its rows land, fill D_j and LSE_j
+            if (fill_by_consumers) {
+                // a CTA's first unit and the pieces: the consumers, idle until
+                // the rows land, fill D_j and LSE_j in one pass of one row per
+                // thread instead of waiting for this warp's round trips
                 if (lane == 0) mbar_arrive(&aux_bar[s]);
                 continue;
             }
@@ -691,20 +756,22 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     float *scrS = scrP + (size_t)p.max_count * N;
     const int nrounds = (N + R - 1) / R;
     int i = 0;
-    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+    for (int it = blockIdx.x; it < p.n_units; it += gridDim.x, ++i) {
         const int s = i % p.stages;
         if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
         if (!mbar_wait(&aux_bar[s], (i / p.stages) & 1)) return;
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         const uint8_t *sQ = st, *sK = st + tens;
         const float *sD = reinterpret_cast<const float *>(st + 4 * tens), *sL = sD + N;
+        const int u = bwd_item_unit(p, it);
+        const bool piece = !GT && it >= p.n_keep;   // the plan splits no unit with the global token
         const int h = u % tab.H;
         const int t0 = tab.start[h], t1 = tab.start[h + 1];
         const size_t row0 = (size_t)u * N;
-        if (i == 0) {
-            // the first unit's D_j = <dO_j, O_j> and LSE_j (log2 units), one
-            // row per consumer thread: the producer warp would take all the
-            // rows' global-load round trips in turn while every consumer waits
+        if (i == 0 || piece) {
+            // D_j = <dO_j, O_j> and LSE_j (log2 units), one row per consumer
+            // thread: the producer warp would take all the rows' global-load
+            // round trips in turn while every consumer waits
             float *wD = reinterpret_cast<float *>(smem + (size_t)s * p.stage_bytes + 4 * tens), *wL = wD + N;
             for (int j = cw * 32 + lane; j < N; j += cthreads) {
                 wD[j] = row_dot_global_shared(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim,
@@ -712,6 +779,57 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 wL[j] = p.LSE[row0 + j] * kLog2e;
             }
             consumer_sync(cthreads);
+        }
+        if (piece) {
+            // rounds [r0, r1) of this unit: warps 0 .. n-1 take the query
+            // rounds (phase A), warps n .. 2n-1 the key rounds with P and dS
+            // recomputed (phase B), concurrently
+            const int q = (it - p.n_keep) % p.pieces;
+            const int r0 = q * p.piece_rounds, r1 = min(nrounds, r0 + p.piece_rounds);
+            const int n = r1 - r0;
+            if (cw < n) {
+                const int r = r0 + cw;
+                const int jl = r * R + lane / G;
+                const bool valid = jl < N;
+                const int j = valid ? jl : N - 1;
+                int tb = t0, te = t0;
+                if (t1 > t0) round_range(s_off, N, t0, t1, r * R, min(N, r * R + R) - 1, tb, te);
+                S qr, g;
+                qr.load(sQ + (size_t)j * RB, lg.c);
+                g.load(sQ + 3 * tens + (size_t)j * RB, lg.c);
+                float2 dq[32 / G];
+#pragma unroll
+                for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
+                bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (ptrdiff_t)tens, qr, g, sD[j], sL[j],
+                                    p.scale_log2, lg, scrP, scrS, dq);
+                if (valid) {
+#pragma unroll
+                    for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
+                    S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
+                }
+            } else if (cw < 2 * n) {
+                const int r = r0 + cw - n;
+                const int kl = r * R + lane / G;
+                const bool valid = kl < N;
+                const int k = valid ? kl : N - 1;
+                int tb = t0, te = t0;
+                if (t1 > t0) round_range(s_off, N, t0, t1, r * R, min(N, r * R + R) - 1, tb, te);
+                float2 dk[32 / G], dv[32 / G];
+#pragma unroll
+                for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
+                float2 *pw = reinterpret_cast<float2 *>(smem + p.piece_off) + (size_t)(cw - n) * R * p.max_count;
+                bwd_b_recompute_offsets<T, G>(s_off, N, tb, te, k, valid, sQ, sK, (ptrdiff_t)tens, sD, sL,
+                                              p.scale_log2, lg, pw, dk, dv);
+                if (valid) {
+#pragma unroll
+                    for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
+                    S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
+                    S::store(static_cast<T *>(p.dV) + (row0 + k) * kHeadDim, lg.c, dv);
+                }
+            }
+            consumer_sync(cthreads);   // stage free
+            if (cw == 0 && lane == 0) mbar_arrive(&empty_bar[s]);
+            continue;
         }
         // ---- phase A: query rows
         for (int r = cw; r < nrounds; r += p.cwarps) {
@@ -1076,19 +1194,45 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->unroll = 1;
     pl->maxt = maxt;
     pl->prefetch = 0;
-    pl->n_keep = 0;
-    pl->qsub = 1;
-    pl->sub_rows = N;
     pl->qsplit = 1;
     pl->chunk = N;
     pl->kv_cap = N;
     pl->stages = stages;
     pl->groups = 1;
     pl->gwarps = std::max(1, std::min(rounds, maxw - 1));
+    pl->grid = (int)std::min<long>((long)B * tab.H, sms);
     pl->stage_bytes = stage;
     pl->smem = stage * stages + scratch;
+    // The partial last wave: its units cut into pieces of one or two rounds
+    // (each run by 2 or 4 warps of a CTA, phase B recomputing P and dS) when
+    // the pieces fit in one wave of CTAs; otherwise whole units.
+    const int units = B * tab.H;
+    const int left = units % pl->grid;
+    pl->n_keep = units;
+    pl->qsub = 1;       // pieces per unit
+    pl->sub_rows = rounds;   // rounds per piece
+    bool pieces = left > 0 && units > pl->grid && !tab.global0;
+    if (const char *e = getenv("FIBATT_BWD_PIECES")) pieces = pieces && atoi(e) != 0;
+    pl->split_off = 0;
+    if (pieces) {
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        const size_t static_smem = 2048 + sizeof(int) * kMaxEntries;   // barriers + offsets, rounded up
+        for (int pr = 1; pr <= 2; ++pr) {
+            const int np = (rounds + pr - 1) / pr;
+            const size_t area = (size_t)pr * R * std::max(1, tab.max_count) * 8;   // (P, dS) per phase-B warp
+            if ((long)left * np <= pl->grid && 2 * pr <= pl->gwarps &&
+                pl->smem + area + static_smem <= (size_t)optin) {
+                pl->n_keep = units - left;
+                pl->qsub = np;
+                pl->sub_rows = pr;
+                pl->split_off = pl->smem;
+                pl->smem += area;
+                break;
+            }
+        }
+    }
     pl->threads = 32 * (1 + pl->gwarps);
-    pl->grid = (int)std::min<long>((long)B * tab.H, sms);
     return true;
 }
 
@@ -1112,9 +1256,11 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
         if (e != cudaSuccess) return e;
         g_bwd_smem_set[ki][dev] = pl.smem;
     }
+    const int items = pl.n_keep + (units - pl.n_keep) * pl.qsub;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                units, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
-                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch()};
+                items, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
+                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch(),
+                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -1127,7 +1273,7 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0};
+                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0, a.B * tab.H, 1, 1, 0};
     const dim3 grid((unsigned)count, (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
     float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N

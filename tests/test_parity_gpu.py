@@ -133,6 +133,18 @@ def test_resident_last_wave_pieces(split, monkeypatch):
     _fwd_full(wl, seed=13)
 
 
+@pytest.mark.parametrize("pieces", ["0", "1"])
+@pytest.mark.parametrize("B", [13, 14])
+def test_resident_bwd_last_wave_pieces(B, pieces, monkeypatch):
+    # 156 or 168 heads on (at most) 152 CTAs: the 4 or 16 heads of the
+    # partial last wave are cut into pieces of one or two rounds, each piece
+    # recomputing P and dS for its key rows; every gradient of every head
+    # compared with the oracle
+    monkeypatch.setenv("FIBATT_PATH", "resident")
+    monkeypatch.setenv("FIBATT_BWD_PIECES", pieces)
+    _bwd_full(WORKLOADS["vitb"].with_batch(B), seed=B)
+
+
 @pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
 @pytest.mark.parametrize("scale", [0.0, 1e-3, -0.5, 3.0])
 def test_extreme_scales(scale, kernel_path):
