@@ -577,7 +577,7 @@ template <typename T, int G>
 __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int tb, int te, int j, bool valid,
                                               const uint8_t *sK, ptrdiff_t vdelta, const Slice<T, G> &q,
                                               const Slice<T, G> &g, float Dj, float lse2, float sl2,
-                                              const LaneGeom<T, G> &lg, float *scrP, float *scrS,
+                                              const LaneGeom<T, G> &lg, float2 *scr,
                                               float2 (&dq)[32 / G]) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
@@ -594,8 +594,7 @@ __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int
         const float P = in ? fast_exp2(fmaf(s, sl2, -lse2)) : 0.f;
         const float dS = P * (dp - Dj);
         if (writer && in) {
-            scrP[(t - t0) * N + j] = P;
-            scrS[(t - t0) * N + j] = dS;
+            scr[(t - t0) * N + j] = make_float2(P, dS);
         }
         kk.axpy(dS, dq);
     }
@@ -606,7 +605,7 @@ __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int
 template <typename T, int G>
 __device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int t1, int tb, int te, int k,
                                               bool valid, const uint8_t *sQ, ptrdiff_t gdelta,
-                                              const LaneGeom<T, G> &lg, const float *scrP, const float *scrS,
+                                              const LaneGeom<T, G> &lg, const float2 *scr,
                                               float2 (&dk)[32 / G], float2 (&dv)[32 / G]) {
     using S = Slice<T, G>;
     constexpr int RB = S::kRowBytes;
@@ -615,8 +614,9 @@ __device__ __forceinline__ void bwd_b_offsets(const int *off, int N, int t0, int
         const bool in = valid && j >= 0 && j < N;
         const int jc = min(max(j, 0), N - 1);
         const int m = t0 + t1 - 1 - t;            // forward offset index of the pair (j, k)
-        const float P = in ? scrP[(m - t0) * N + jc] : 0.f;
-        const float dS = in ? scrS[(m - t0) * N + jc] : 0.f;
+        const float2 w = scr[(m - t0) * N + jc];   // a stale pair when out of range: masked below
+        const float P = in ? w.x : 0.f;
+        const float dS = in ? w.y : 0.f;
         const uint8_t *a = sQ + (ptrdiff_t)jc * RB;
         S qq, gg;
         qq.load(a, lg.c);
@@ -752,8 +752,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     if (cw >= p.cwarps) return;
     const int cthreads = 32 * p.cwarps;
     const LaneGeom<T, G> lg;
-    float *scrP = reinterpret_cast<float *>(smem + p.scratch_off);
-    float *scrS = scrP + (size_t)p.max_count * N;
+    float2 *scr = reinterpret_cast<float2 *>(smem + p.scratch_off);   // (P, dS) [offset][row]
     const int nrounds = (N + R - 1) / R;
     int i = 0;
     for (int it = blockIdx.x; it < p.n_units; it += gridDim.x, ++i) {
@@ -801,7 +800,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
                 bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (ptrdiff_t)tens, qr, g, sD[j], sL[j],
-                                    p.scale_log2, lg, scrP, scrS, dq);
+                                    p.scale_log2, lg, scr, dq);
                 if (valid) {
 #pragma unroll
                     for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
@@ -848,7 +847,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
             bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg,
-                                scrP, scrS, dq);
+                                scr, dq);
             if constexpr (GT)
                 bwd_a_global<T, G>(s_off, t0, t1, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg, dq);
             if (valid && !(GT && j == 0)) {   // dQ_0: dense-row kernel
@@ -869,7 +868,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             float2 dk[32 / G], dv[32 / G];
 #pragma unroll
             for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
-            bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (ptrdiff_t)(3 * tens), lg, scrP, scrS, dk,
+            bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (ptrdiff_t)(3 * tens), lg, scr, dk,
                                 dv);
             if constexpr (GT)
                 bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)u * 2 * N, N, sQ, (ptrdiff_t)(3 * tens),
@@ -905,8 +904,7 @@ __device__ __forceinline__ void bwd_flat_a_round(const TableArg &tab, const BwdP
     const size_t row0 = (size_t)bh * N;
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB;
     const ptrdiff_t vdelta = static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.K);
-    float *scrP = scr;   // this unit's weights
-    float *scrS = scrP + (size_t)p.max_count * N;
+    float2 *scr2 = reinterpret_cast<float2 *>(scr);   // this unit's (P, dS) [offset][row]
     const LaneGeom<T, G> lg;
     const int jl = r * R + lane / G;
     const bool valid = jl < N;
@@ -923,7 +921,7 @@ __device__ __forceinline__ void bwd_flat_a_round(const TableArg &tab, const BwdP
     float2 dq[32 / G];
 #pragma unroll
     for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
-    bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, scrP, scrS,
+    bwd_a_offsets<T, G>(s_off, N, t0, tb, te, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, scr2,
                         dq);
     if constexpr (GT) bwd_a_global<T, G>(s_off, t0, t1, j, valid, gK, vdelta, q, g, Dj, lse2, p.scale_log2, lg, dq);
     if (valid && !(GT && j == 0)) {
@@ -971,8 +969,7 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
     const size_t row0 = (size_t)bh * N;
     const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB;
     const ptrdiff_t gdelta = static_cast<const uint8_t *>(p.dO) - static_cast<const uint8_t *>(p.Q);
-    const float *scrP = scr + (size_t)blockIdx.x * 2 * p.max_count * N;   // this unit's weights
-    const float *scrS = scrP + (size_t)p.max_count * N;
+    const float2 *scr2 = reinterpret_cast<const float2 *>(scr + (size_t)blockIdx.x * 2 * p.max_count * N);
     const LaneGeom<T, G> lg;
     const int kl = r * R + lane / G;
     const bool valid = kl < N;
@@ -983,7 +980,7 @@ bwd_flat_b_kernel(const __grid_constant__ TableArg tab, const BwdParams p, const
     float2 dk[32 / G], dv[32 / G];
 #pragma unroll
     for (int x = 0; x < 32 / G; ++x) dk[x] = dv[x] = make_float2(0.f, 0.f);
-    bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, gQ, gdelta, lg, scrP, scrS, dk, dv);
+    bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, gQ, gdelta, lg, scr2, dk, dv);
     if constexpr (GT) bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)bh * 2 * N, N, gQ, gdelta, lg, dk, dv);
     if (valid && !(GT && k == 0)) {
 #pragma unroll
