@@ -64,7 +64,21 @@ struct PipeParams {
     int qsub;
     int sub_rows;
     int early_prefetch;   // L2-prefetch the first units before the grid-dependency wait
+    int snake;            // odd full waves take the CTAs in reverse order
 };
+
+// Unit of this CTA's slot k (-1 past the end).  Slot k of CTA c is wave k,
+// position c; with `snake`, odd full waves run the positions backwards, so a
+// CTA alternates between the two ends of each wave (query chunks and heads
+// otherwise repeat with the wave, since the grid and the units per batch
+// element share factors).
+__device__ __forceinline__ int fwd_slot_unit(const PipeParams &p, int k) {
+    const int c = (int)blockIdx.x, g = (int)gridDim.x;
+    const long L = (long)k * g + c;
+    if (L >= p.n_units) return -1;
+    if (p.snake && (k & 1) && (long)(k + 1) * g <= p.n_keep) return k * g + (g - 1 - c);
+    return (int)L;
+}
 
 struct Unit {
     int bh, h, q0, q1, t0, t1, lo, nrows;
@@ -324,8 +338,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         // copies issued after the grid-dependency wait below still read what
         // the previous kernel wrote.
         for (int i = 0; i < p.stages; ++i) {
-            const int u = (int)blockIdx.x + i * (int)gridDim.x;
-            if (u < p.n_units) prefetch_unit<T>(tab, p, u);
+            const int u = fwd_slot_unit(p, i);
+            if (u >= 0) prefetch_unit<T>(tab, p, u);
         }
     }
     for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
@@ -348,13 +362,14 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         // producer: one lane streams every unit of this CTA into the ring and
         // keeps the next `prefetch` units warming in L2
         if (lane != 0) return;
-        int i = 0;
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+        for (int i = 0;; ++i) {
+            const int u = fwd_slot_unit(p, i);
+            if (u < 0) break;
             const int s = i % p.stages;
             if (i == 0)
                 for (int d = p.stages; d < p.stages + p.prefetch; ++d) {
-                    const int un = u + d * gridDim.x;
-                    if (un < p.n_units) prefetch_unit<T>(tab, p, un);
+                    const int un = fwd_slot_unit(p, d);
+                    if (un >= 0) prefetch_unit<T>(tab, p, un);
                 }
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
             const Unit g = unit_geometry(tab, p, u);
@@ -373,8 +388,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
                 bulk_g2s(st + g0_off + RB, static_cast<const T *>(p.V) + row0 * kHeadDim, RB, &full_bar[s]);
             }
             if (i >= 1 && p.prefetch > 0) {
-                const int un = u + (p.stages + p.prefetch - 1) * gridDim.x;
-                if (un < p.n_units) prefetch_unit<T>(tab, p, un);
+                const int un = fwd_slot_unit(p, i + p.stages + p.prefetch - 1);
+                if (un >= 0) prefetch_unit<T>(tab, p, un);
             }
         }
         return;
@@ -391,8 +406,9 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     if (grp >= p.groups) return;
     const LaneGeom<T, G> lg;
     const int rpu = p.chunk / R;
-    int i = grp;
-    for (int u = blockIdx.x + grp * gridDim.x; u < p.n_units; u += p.groups * gridDim.x, i += p.groups) {
+    for (int i = grp;; i += p.groups) {
+        const int u = fwd_slot_unit(p, i);
+        if (u < 0) break;
         const int s = i % p.stages, k = i / p.stages;
         if (k >= 1 && !mbar_wait(&empty_bar[s], (k - 1) & 1)) return;
         if (!mbar_wait(&full_bar[s], k & 1)) return;
@@ -1002,6 +1018,13 @@ int early_prefetch() {
     return on && pdl_enabled();
 }
 
+// Snake order of the forward's waves (FIBATT_FWD_SNAKE=0 turns it off; read
+// per call, so a test can compare both orders in one process).
+static int fwd_snake() {
+    const char *e = getenv("FIBATT_FWD_SNAKE");
+    return (e && atoi(e) == 0) ? 0 : 1;
+}
+
 int g_sm_count[64] = {0};
 size_t g_fwd_smem_set[32][64] = {{0}};
 size_t g_bwd_smem_set[16][64] = {{0}};
@@ -1145,7 +1168,8 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     const int n_reg = a.B * a.tab->H * pl.qsplit;
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
                  pl.n_keep + (n_reg - pl.n_keep) * pl.qsub, pl.stages, pl.groups, pl.gwarps,
-                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows, early_prefetch()};
+                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows, early_prefetch(),
+                 fwd_snake()};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);

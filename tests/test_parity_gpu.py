@@ -121,15 +121,18 @@ def test_resident_query_chunks(qsplit, dtype, monkeypatch):
     _fwd_full(wl, seed=23)
 
 
+@pytest.mark.parametrize("snake", ["0", "1"])
 @pytest.mark.parametrize("split", ["0", "1"])
-def test_resident_last_wave_pieces(split, monkeypatch):
-    # 7 x 12 heads x 2 chunks = 168 units on (at most) 152 CTAs: the units of
-    # the partial last wave are cut into one-round pieces, some of them past
-    # the end of their chunk (empty)
+def test_resident_last_wave_pieces(split, snake, monkeypatch):
+    # with the split: 7 x 12 heads x 2 chunks = 168 units on (at most) 152
+    # CTAs, the units of the partial last wave cut into one-round pieces, some
+    # of them past the end of their chunk (empty); without: 20 x 24 = 480
+    # units, three full waves, the second of them reversed by the snake order
     monkeypatch.setenv("FIBATT_PATH", "resident")
     monkeypatch.setenv("FIBATT_QSPLIT", "2")
     monkeypatch.setenv("FIBATT_SPLIT_TAIL", split)
-    wl = WORKLOADS["vitb"].with_batch(7)
+    monkeypatch.setenv("FIBATT_FWD_SNAKE", snake)
+    wl = WORKLOADS["vitb"].with_batch(7 if split == "1" else 20)
     _fwd_full(wl, seed=13)
 
 
