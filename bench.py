@@ -105,6 +105,14 @@ def algorithmic_bytes(wl, backward: bool) -> int:
     return (8 * e * s + 4 * rows) if backward else (4 * e * s + 4 * rows)
 
 
+# Secondary roofline: FP32 arithmetic.  Per attended pair the forward does
+# 2 x 64 multiply-adds (the score and the row update), the backward 5 x 64
+# (two scores, three row updates); the peak is the GB300's FP32 FMA rate,
+# 152 SMs x 128 lanes x 2 flops at the 2070 MHz maximum SM clock.
+FLOPS_PER_PAIR = {"fwd": 2 * 2 * 64, "bwd": 5 * 2 * 64}
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -454,6 +462,11 @@ def gb300_arm(args):
                 "frac": round(d_bytes / d_ms / 1e6 / peak, 4),
                 "traffic": recorded_traffic(kname, wl.name),
                 "algorithmic_bytes": d_bytes, "avg_ms": round(d_ms, 5)}
+    d_tflops = step.pairs * FLOPS_PER_PAIR[dominant] / (d_ms / 1e3) / 1e12   # one GPU, like the HBM line
+    roofline_alu = {"bound": "alu", "kernel": kname, "achieved": round(d_tflops, 2),
+                    "peak": round(FP32_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
+                    "frac": round(d_tflops / FP32_PEAK_TFLOPS, 4),
+                    "flops_per_pair": FLOPS_PER_PAIR[dominant]}
 
     e2e_ms, h2d, d2h = run_e2e(step, dev, args.e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
@@ -481,6 +494,7 @@ def gb300_arm(args):
                     "GB_s": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6, 1),
                     "frac_hbm": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6 / peak, 4)},
         "roofline": roofline,
+        "roofline_alu": roofline_alu,
         "e2e": {"value": world * step.pairs / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": args.e2e_steps},
