@@ -1065,8 +1065,9 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     int dev = 0;
     cudaGetDevice(&dev);
     const int sms = sm_count(dev);
-    // two lanes per row measured fastest on the ViT-B shape (tuning overrides below)
-    int G = 2, unroll = 2, maxt = 1024;
+    // two lanes per row, one offset per step, measured fastest on the ViT-B
+    // shapes with whole-head units (tuning overrides below)
+    int G = 2, unroll = 1, maxt = 1024;
     if (const char *e = getenv("FIBATT_LANES")) G = atoi(e) == 2 ? 2 : 4;
     if (G == 2) maxt = 512;
     if (const char *e = getenv("FIBATT_UNROLL")) unroll = atoi(e) == 1 ? 1 : 2;
@@ -1079,15 +1080,17 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     }
     const int R = 32 / G;                                  // rows per warp round
     const int maxw = maxt / 32;
-    // Query chunks of a multiple of R rows.  Aim for >= 8 units per SM and a
-    // ring of at least three stages.
+    // Query chunks of a multiple of R rows.  Whole heads when there are at
+    // least as many heads as SMs (each K/V window is then loaded once and a
+    // unit's rounds fill the CTA's warps), else enough chunks to give every
+    // SM a unit; and a ring of at least two stages.
     int qsplit = 1;
     const char *env = getenv("FIBATT_QSPLIT");
     if (env) {
         qsplit = std::max(1, atoi(env));
     } else {
         const long units = (long)B * tab.H;
-        while (qsplit < 64 && units * qsplit < 8L * sms && (N + qsplit) / (qsplit + 1) >= 32) ++qsplit;
+        while (qsplit < 64 && units * qsplit < sms && (N + qsplit) / (qsplit + 1) >= 32) ++qsplit;
     }
     // Smallest possible stage (one round of rows): if even that does not fit,
     // the windows are too wide for this kernel.
@@ -1098,13 +1101,13 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     }
     int chunk = 0, kv_cap = 0;
     size_t stage = 0;
-    // grow the split geometrically until three stages fit (or rows run out)
+    // grow the split geometrically until two stages fit (or rows run out)
     for (;; qsplit = std::max(qsplit + 1, qsplit * 5 / 4)) {
         chunk = ((N + qsplit - 1) / qsplit + R - 1) / R * R;
         const int qs = (N + chunk - 1) / chunk;
         kv_cap = window_cap(tab, qs, chunk);
         stage = ((size_t)chunk * RB + 2 * (size_t)kv_cap * RB + (tab.global0 ? 2 * RB : 0) + 127) / 128 * 128;
-        if (env || 3 * stage <= budget || chunk <= R) {
+        if (env || 2 * stage <= budget || chunk <= R) {
             qsplit = qs;
             break;
         }
@@ -1113,10 +1116,12 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     if (stages < 1) return false;
     if (const char *e = getenv("FIBATT_STAGES")) stages = std::max(1, std::min(stages, atoi(e)));
     // consumer groups: at most two (the kernel's release-then-full wait needs
-    // groups <= 2, or stages a multiple of groups)
-    int groups = stages >= 2 ? 2 : 1;
-    if (const char *e = getenv("FIBATT_GROUPS")) groups = std::max(1, std::min(2, atoi(e)));
+    // groups <= 2, or stages a multiple of groups), and two only when a
+    // unit's rounds leave warps for a second group; one group keeps a whole
+    // stage of lead on every load
     const int rounds = chunk / R;
+    int groups = stages >= 2 && 2 * rounds <= maxw - 1 ? 2 : 1;
+    if (const char *e = getenv("FIBATT_GROUPS")) groups = std::max(1, std::min(2, atoi(e)));
     const int gwarps = std::max(1, std::min(rounds, (maxw - 1) / groups));
     int prefetch = 0;   // L2 warming of later units measured slower: off by default
     if (const char *e = getenv("FIBATT_PREFETCH")) prefetch = std::max(0, std::min(8, atoi(e)));
