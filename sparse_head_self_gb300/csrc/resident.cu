@@ -533,10 +533,17 @@ struct BwdParams {
     int pieces;
     int piece_rounds;
     uint32_t piece_off;   // per phase-B warp of a piece: [max_count][R] (P, dS) pairs
+    int snake;            // odd full waves take the CTAs in reverse order (as the forward)
 };
 
+// Unit of item u: item c + k * grid is wave k, position c; with `snake` odd
+// full waves run the positions backwards (see fwd_slot_unit); the items past
+// n_keep are pieces of the last units, in order.
 __device__ __forceinline__ int bwd_item_unit(const BwdParams &p, int u) {
-    return u < p.n_keep ? u : p.n_keep + (u - p.n_keep) / p.pieces;
+    if (u >= p.n_keep) return p.n_keep + (u - p.n_keep) / p.pieces;
+    const int g = (int)gridDim.x, k = u / g;
+    if (p.snake && (k & 1) && (k + 1) * g <= p.n_keep) return k * g + (g - 1 - u % g);
+    return u;
 }
 
 // Phase B for one round of key rows with P and dS recomputed from the staged
@@ -1025,6 +1032,12 @@ static int fwd_snake() {
     return (e && atoi(e) == 0) ? 0 : 1;
 }
 
+// The same for the resident backward (FIBATT_BWD_SNAKE=0 turns it off).
+static int bwd_snake() {
+    const char *e = getenv("FIBATT_BWD_SNAKE");
+    return (e && atoi(e) == 0) ? 0 : 1;
+}
+
 int g_sm_count[64] = {0};
 size_t g_fwd_smem_set[32][64] = {{0}};
 size_t g_bwd_smem_set[16][64] = {{0}};
@@ -1286,7 +1299,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 items, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
                 (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch(),
-                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off};
+                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off, bwd_snake()};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -1299,7 +1312,7 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0, a.B * tab.H, 1, 1, 0};
+                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0, a.B * tab.H, 1, 1, 0, 0};
     const dim3 grid((unsigned)count, (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
     float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N

@@ -137,12 +137,13 @@ def test_resident_last_wave_pieces(split, snake, monkeypatch):
 
 
 @pytest.mark.parametrize("pieces", ["0", "1"])
-@pytest.mark.parametrize("B", [13, 14])
+@pytest.mark.parametrize("B", [13, 14, 27])
 def test_resident_bwd_last_wave_pieces(B, pieces, monkeypatch):
-    # 156 or 168 heads on (at most) 152 CTAs: the 4 or 16 heads of the
-    # partial last wave are cut into pieces of one or two rounds, each piece
-    # recomputing P and dS for its key rows; every gradient of every head
-    # compared with the oracle
+    # 156, 168 or 324 heads on (at most) 152 CTAs: the 4, 16 or 20 heads of
+    # the partial last wave are cut into pieces of one or two rounds, each
+    # piece recomputing P and dS for its key rows (B = 27: two full waves, the
+    # second in snake order); every gradient of every head compared with the
+    # oracle
     monkeypatch.setenv("FIBATT_PATH", "resident")
     monkeypatch.setenv("FIBATT_BWD_PIECES", pieces)
     _bwd_full(WORKLOADS["vitb"].with_batch(B), seed=B)
