@@ -132,6 +132,21 @@ def test_global_token_unsupported_paths_fail_before_launch(monkeypatch):
                                 None) == 2
 
 
+def test_entry_limit_is_exact():
+    # FIBATT_MAX_ENTRIES signed entries in total are accepted, one more is not
+    L = _native.lib()
+    h = ctypes.c_void_p()
+    limit = 1024
+    d = list(range(1, limit // 2 + 1))   # 512 distances -> 1024 signed entries without the diagonal
+    assert L.fibatt_support_build_distances(1, 2000, api._i32([len(d)]), api._i32(d), 0, ctypes.byref(h)) == 0
+    n, N, total = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    assert L.fibatt_support_info(h, ctypes.byref(n), ctypes.byref(N), ctypes.byref(total)) == 0
+    assert total.value == limit
+    L.fibatt_support_destroy(h)
+    assert L.fibatt_support_build_distances(1, 2000, api._i32([len(d)]), api._i32(d), 1, ctypes.byref(h)) == 2
+    assert "more than 1024 signed offsets" in L.fibatt_last_error().decode()
+
+
 def test_permutation_reorders_heads():
     base = api.Support.wythoff(4, 100, 5, 100, True)
     perm = [2, 0, 3, 1]
