@@ -95,6 +95,7 @@ struct ResidentPlan {
     int qsub;            // pieces each last-wave unit is cut into
     int sub_rows;        // forward: query rows per piece; backward: rounds per piece
     size_t split_off;    // backward: byte offset of the pieces' (P, dS) areas
+    int piece_par;       // backward: one-round pieces spread over more warps
     size_t stage_bytes;  // bytes per ring stage
     size_t smem;         // dynamic shared memory bytes
     int threads;         // threads per CTA (producer warp + consumers)

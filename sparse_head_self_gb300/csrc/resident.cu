@@ -534,7 +534,11 @@ struct BwdParams {
     int piece_rounds;
     uint32_t piece_off;   // per phase-B warp of a piece: [max_count][R] (P, dS) pairs
     int snake;            // odd full waves take the CTAs in reverse order (as the forward)
+    int piece_par;        // one-round pieces spread over kPieceA + kPieceB warps (see the kernel)
 };
+
+constexpr int kPieceA = 3;   // warps on a piece's query round, a third of its offsets each
+constexpr int kPieceB = 6;   // warps on the first pass of its key round, a sixth each
 
 // Unit of item u: item c + k * grid is wave k, position c; with `snake` odd
 // full waves run the positions backwards (see fwd_slot_unit); the items past
@@ -544,6 +548,71 @@ __device__ __forceinline__ int bwd_item_unit(const BwdParams &p, int u) {
     const int g = (int)gridDim.x, k = u / g;
     if (p.snake && (k & 1) && (k + 1) * g <= p.n_keep) return k * g + (g - 1 - u % g);
     return u;
+}
+
+// acc (this lane's slice of a row, in its chunk order) stored to a fp32 row of
+// 64 dims in shared memory.
+template <typename T, int G>
+__device__ __forceinline__ void acc_store_shared(float *row, const int (&c)[Slice<T, G>::kChunks],
+                                                 const float2 (&acc)[32 / G]) {
+    constexpr int kPerChunk = 16 / (int)sizeof(T) / 2;   // element pairs per 16-byte chunk
+#pragma unroll
+    for (int i = 0; i < Slice<T, G>::kChunks; ++i) {
+        const int base = c[i] / (int)sizeof(T);
+#pragma unroll
+        for (int e = 0; e < kPerChunk; e += 2)
+            *reinterpret_cast<float4 *>(row + base + 2 * e) =
+                make_float4(acc[kPerChunk * i + e].x, acc[kPerChunk * i + e].y, acc[kPerChunk * i + e + 1].x,
+                            acc[kPerChunk * i + e + 1].y);
+    }
+}
+
+// acc += the fp32 row of 64 dims at `row` in shared memory (this lane's slice,
+// in its chunk order): the inverse of acc_store_shared.
+template <typename T, int G>
+__device__ __forceinline__ void acc_add_from_shared(const float *row, const int (&c)[Slice<T, G>::kChunks],
+                                                    float2 (&acc)[32 / G]) {
+    constexpr int kPerChunk = 16 / (int)sizeof(T) / 2;
+#pragma unroll
+    for (int i = 0; i < Slice<T, G>::kChunks; ++i) {
+        const int base = c[i] / (int)sizeof(T);
+#pragma unroll
+        for (int e = 0; e < kPerChunk; e += 2) {
+            const float4 v = *reinterpret_cast<const float4 *>(row + base + 2 * e);
+            acc[kPerChunk * i + e] = add2(acc[kPerChunk * i + e], make_float2(v.x, v.y));
+            acc[kPerChunk * i + e + 1] = add2(acc[kPerChunk * i + e + 1], make_float2(v.z, v.w));
+        }
+    }
+}
+
+// First pass of a piece's key round over offsets [ta, tz): (P, dS) of the
+// pairs (k + off, k) from the staged rows into pw[(t - tb) R + row].
+template <typename T, int G>
+__device__ __forceinline__ void bwd_b_weights(const int *off, int N, int tb, int ta, int tz, int k, bool valid,
+                                              const uint8_t *sQ, const uint8_t *sK, ptrdiff_t tens,
+                                              const float *sD, const float *sL, float sl2,
+                                              const LaneGeom<T, G> &lg, float2 *pw) {
+    using S = Slice<T, G>;
+    constexpr int RB = S::kRowBytes;
+    constexpr int R = 32 / G;
+    const int lane = threadIdx.x & 31, row = lane / G;
+    const bool writer = (lane & (G - 1)) == 0;
+    S kk, vv;
+    kk.load(sK + (ptrdiff_t)k * RB, lg.c);
+    vv.load(sK + tens + (ptrdiff_t)k * RB, lg.c);
+    for (int t = ta; t < tz; ++t) {
+        const int j = k + off[t];
+        const bool in = valid && j >= 0 && j < N;
+        const int jc = min(max(j, 0), N - 1);
+        const uint8_t *a = sQ + (ptrdiff_t)jc * RB;
+        S qq, gg;
+        qq.load(a, lg.c);
+        gg.load(a + 3 * tens, lg.c);
+        const float sc = group_sum<G>(qq.dot(kk));
+        const float dp = group_sum<G>(gg.dot(vv));
+        const float P = in ? fast_exp2(fmaf(sc, sl2, -sL[jc])) : 0.f;
+        if (writer) pw[(t - tb) * R + row] = make_float2(P, P * (dp - sD[jc]));
+    }
 }
 
 // Phase B for one round of key rows with P and dS recomputed from the staged
@@ -596,7 +665,7 @@ __device__ __forceinline__ void bwd_b_recompute_offsets(const int *off, int N, i
 // Phase A for one round of query rows, branch-free: the key row is clamped
 // into [0, N) and an out-of-range pair gets P = 0 (so dS = 0 too); only
 // in-range pairs are written to the scratch.
-template <typename T, int G>
+template <typename T, int G, bool STORE = true>
 __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int tb, int te, int j, bool valid,
                                               const uint8_t *sK, ptrdiff_t vdelta, const Slice<T, G> &q,
                                               const Slice<T, G> &g, float Dj, float lse2, float sl2,
@@ -616,9 +685,7 @@ __device__ __forceinline__ void bwd_a_offsets(const int *off, int N, int t0, int
         const float dp = group_sum<G>(g.dot(vv));
         const float P = in ? fast_exp2(fmaf(s, sl2, -lse2)) : 0.f;
         const float dS = P * (dp - Dj);
-        if (writer && in) {
-            scr[(t - t0) * N + j] = make_float2(P, dS);
-        }
+        if (STORE && writer && in) scr[(t - t0) * N + j] = make_float2(P, dS);
         kk.axpy(dS, dq);
     }
 }
@@ -730,7 +797,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             const int s = i % p.stages;
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
-            const bool fill_by_consumers = i == 0 || (!GT && it >= p.n_keep);
+            const bool fill_by_consumers = i == 0;
             const size_t row0 = (size_t)bwd_item_unit(p, it) * N;
             if (lane == 0) {
                 const uint32_t b = (uint32_t)tens;
@@ -753,18 +820,33 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             }
             __syncwarp();
             if (fill_by_consumers) {
-                // a CTA's first unit and the pieces: the consumers, idle until
-                // the rows land, fill D_j and LSE_j in one pass of one row per
-                // thread instead of waiting for this warp's round trips
+                // a CTA's first unit: the consumers, idle until the rows land,
+                // fill D_j and LSE_j in one pass of one row per thread instead
+                // of waiting for this warp's round trips (later units, pieces
+                // included, have a whole unit of lead for them here)
                 if (lane == 0) mbar_arrive(&aux_bar[s]);
                 continue;
             }
             if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
             float *sD = reinterpret_cast<float *>(st + 4 * tens), *sL = sD + N;
-            for (int j = lane; j < N; j += 32) {
-                sD[j] = row_dot_global_shared(static_cast<const T *>(p.O) + (row0 + j) * kHeadDim,
-                                              st + 3 * tens + (size_t)j * RB, lane);
-                sL[j] = p.LSE[row0 + j] * kLog2e;
+            // kDRows rows per lane and step, every dot product formed before
+            // any store, so the rows' global loads are in flight together
+            constexpr int kDRows = 4;
+            for (int j = lane; j < N; j += 32 * kDRows) {
+                float d[kDRows], l[kDRows];
+#pragma unroll
+                for (int x = 0; x < kDRows; ++x) {
+                    const int jx = min(j + 32 * x, N - 1);
+                    d[x] = row_dot_global_shared(static_cast<const T *>(p.O) + (row0 + jx) * kHeadDim,
+                                                 st + 3 * tens + (size_t)jx * RB, lane);
+                    l[x] = p.LSE[row0 + jx];
+                }
+#pragma unroll
+                for (int x = 0; x < kDRows; ++x)
+                    if (j + 32 * x < N) {
+                        sD[j + 32 * x] = d[x];
+                        sL[j + 32 * x] = l[x] * kLog2e;
+                    }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&aux_bar[s]);
@@ -790,7 +872,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         const int h = u % tab.H;
         const int t0 = tab.start[h], t1 = tab.start[h + 1];
         const size_t row0 = (size_t)u * N;
-        if (i == 0 || piece) {
+        if (i == 0) {
             // D_j = <dO_j, O_j> and LSE_j (log2 units), one row per consumer
             // thread: the producer warp would take all the rows' global-load
             // round trips in turn while every consumer waits
@@ -801,6 +883,90 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 wL[j] = p.LSE[row0 + j] * kLog2e;
             }
             consumer_sync(cthreads);
+        }
+        if (piece && p.piece_par) {
+            // a one-round piece spread over the warps: kPieceA warps take a
+            // share of the query round's offsets each (partial dQ rows in the
+            // scratch area, which pieces do not use otherwise), kPieceB warps
+            // compute the key round's (P, dS) for a share of the offsets each,
+            // then one warp accumulates dK and one dV over all of them.  A
+            // piece is always its CTA's last item (the plan keeps the pieces
+            // within one wave).
+            const int r = (it - p.n_keep) % p.pieces;
+            const int lr = lane / G;
+            int tb = t0, te = t0;
+            if (t1 > t0) round_range(s_off, N, t0, t1, r * R, min(N, r * R + R) - 1, tb, te);
+            const int m = te - tb;
+            float *pa = reinterpret_cast<float *>(smem + p.scratch_off);   // [kPieceA - 1][R][64] partial dQ
+            float2 *pw = reinterpret_cast<float2 *>(smem + p.piece_off);   // [m][R] (P, dS)
+            if (cw < kPieceA) {
+                const int jl = r * R + lr;
+                const bool valid = jl < N;
+                const int j = valid ? jl : N - 1;
+                S qr, g;
+                qr.load(sQ + (size_t)j * RB, lg.c);
+                g.load(sQ + 3 * tens + (size_t)j * RB, lg.c);
+                float2 dq[32 / G];
+#pragma unroll
+                for (int x = 0; x < 32 / G; ++x) dq[x] = make_float2(0.f, 0.f);
+                bwd_a_offsets<T, G, false>(s_off, N, t0, tb + (m * cw) / kPieceA, tb + (m * (cw + 1)) / kPieceA, j,
+                                           valid, sK, (ptrdiff_t)tens, qr, g, sD[j], sL[j], p.scale_log2, lg, scr,
+                                           dq);
+                // warps 1 .. kPieceA-1 hand their partial rows to warp 0,
+                // which adds them (in order) and stores the dQ rows
+                if (cw > 0) acc_store_shared<T, G>(pa + ((size_t)(cw - 1) * R + lr) * kHeadDim, lg.c, dq);
+                named_sync(3, 32 * kPieceA);
+                if (cw == 0) {
+                    for (int a = 0; a < kPieceA - 1; ++a)
+                        acc_add_from_shared<T, G>(pa + ((size_t)a * R + lr) * kHeadDim, lg.c, dq);
+                    if (valid) {
+#pragma unroll
+                        for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
+                        S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
+                    }
+                }
+            } else if (cw < kPieceA + kPieceB) {
+                const int b = cw - kPieceA;
+                const int kl = r * R + lr;
+                const bool valid = kl < N;
+                const int k = valid ? kl : N - 1;
+                bwd_b_weights<T, G>(s_off, N, tb, tb + (m * b) / kPieceB, tb + (m * (b + 1)) / kPieceB, k, valid, sQ,
+                                    sK, (ptrdiff_t)tens, sD, sL, p.scale_log2, lg, pw);
+                named_sync(2, 32 * kPieceB);   // every (P, dS) of the round written
+                if (b < 2) {   // b = 0: dK = scale sum dS q_j; b = 1: dV = sum P dO_j
+                    float2 acc[32 / G];
+#pragma unroll
+                    for (int x = 0; x < 32 / G; ++x) acc[x] = make_float2(0.f, 0.f);
+                    const uint8_t *src = b == 0 ? sQ : sQ + 3 * tens;
+                    int t = tb;
+                    for (; t + 1 < te; t += 2) {   // two offsets per step: their loads overlap
+                        const int j0 = min(max(k + s_off[t], 0), N - 1), j1 = min(max(k + s_off[t + 1], 0), N - 1);
+                        const float2 w0 = pw[(t - tb) * R + lr], w1 = pw[(t + 1 - tb) * R + lr];   // (0, 0) out of range
+                        S r0, r1;
+                        r0.load(src + (size_t)j0 * RB, lg.c);
+                        r1.load(src + (size_t)j1 * RB, lg.c);
+                        r0.axpy(b == 0 ? w0.y : w0.x, acc);
+                        r1.axpy(b == 0 ? w1.y : w1.x, acc);
+                    }
+                    for (; t < te; ++t) {
+                        const int jc = min(max(k + s_off[t], 0), N - 1);
+                        const float2 w = pw[(t - tb) * R + lr];
+                        S rr;
+                        rr.load(src + (size_t)jc * RB, lg.c);
+                        rr.axpy(b == 0 ? w.y : w.x, acc);
+                    }
+                    if (valid) {
+                        if (b == 0) {
+#pragma unroll
+                            for (int x = 0; x < 32 / G; ++x) acc[x] = mul2(acc[x], make_float2(p.scale, p.scale));
+                        }
+                        S::store(static_cast<T *>(b == 0 ? p.dK : p.dV) + (row0 + k) * kHeadDim, lg.c, acc);
+                    }
+                }
+            }
+            consumer_sync(cthreads);   // stage free
+            if (cw == 0 && lane == 0) mbar_arrive(&empty_bar[s]);
+            continue;
         }
         if (piece) {
             // rounds [r0, r1) of this unit: warps 0 .. n-1 take the query
@@ -1253,6 +1419,7 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     bool pieces = left > 0 && units > pl->grid && !tab.global0;
     if (const char *e = getenv("FIBATT_BWD_PIECES")) pieces = pieces && atoi(e) != 0;
     pl->split_off = 0;
+    pl->piece_par = 0;
     if (pieces) {
         int optin = 0;
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -1267,6 +1434,11 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
                 pl->sub_rows = pr;
                 pl->split_off = pl->smem;
                 pl->smem += area;
+                // one-round pieces over kPieceA + kPieceB warps: the partial
+                // dQ rows go to the P/dS scratch, which must hold them
+                pl->piece_par = pr == 1 && pl->gwarps >= kPieceA + kPieceB &&
+                                scratch >= (size_t)kPieceA * R * kHeadDim * sizeof(float);
+                if (const char *e = getenv("FIBATT_BWD_PIECE_PAR")) pl->piece_par = pl->piece_par && atoi(e) != 0;
                 break;
             }
         }
@@ -1299,7 +1471,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 items, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
                 (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch(),
-                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off, bwd_snake()};
+                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off, bwd_snake(), pl.piece_par};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -1312,7 +1484,7 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
-                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0, a.B * tab.H, 1, 1, 0, 0};
+                a.B * tab.H, 0, 0, 0, 0, std::max(1, (int)tab.max_count), a.gw, 0, a.B * tab.H, 1, 1, 0, 0, 0};
     const dim3 grid((unsigned)count, (unsigned)((tab.N + R * W - 1) / (R * W)));
     const bool pdl = pdl_enabled();
     float *scr = a.Dws;   // unit bh0 + x at x * 2 * max_count * N

@@ -61,6 +61,12 @@ __device__ __forceinline__ void consumer_sync(int threads) {
     asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
+// Barrier among `threads` threads on named barrier `id` (2..15; 1 is the
+// consumers').
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Plain arrive (count 1) on `bar`.
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -133,6 +139,8 @@ __device__ __forceinline__ uint32_t bf16x2_splat(float p) {
 }
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 // 2^x on the SFU (ex2.approx.ftz, relative error about 2^-22; results below
 // 2^-126 flush to zero, which only drops weights under 1e-38).

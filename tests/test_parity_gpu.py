@@ -136,7 +136,7 @@ def test_resident_last_wave_pieces(split, snake, monkeypatch):
     _fwd_full(wl, seed=13)
 
 
-@pytest.mark.parametrize("pieces", ["0", "1"])
+@pytest.mark.parametrize("pieces", ["0", "1", "1-serial"])
 @pytest.mark.parametrize("B", [13, 14, 27])
 def test_resident_bwd_last_wave_pieces(B, pieces, monkeypatch):
     # 156, 168 or 324 heads on (at most) 152 CTAs: the 4, 16 or 20 heads of
@@ -144,8 +144,10 @@ def test_resident_bwd_last_wave_pieces(B, pieces, monkeypatch):
     # piece recomputing P and dS for its key rows (B = 27: two full waves, the
     # second in snake order); every gradient of every head compared with the
     # oracle
+    # one-round pieces run spread over nine warps, or ("1-serial") on two
     monkeypatch.setenv("FIBATT_PATH", "resident")
-    monkeypatch.setenv("FIBATT_BWD_PIECES", pieces)
+    monkeypatch.setenv("FIBATT_BWD_PIECES", pieces[0])
+    monkeypatch.setenv("FIBATT_BWD_PIECE_PAR", "0" if pieces.endswith("serial") else "1")
     _bwd_full(WORKLOADS["vitb"].with_batch(B), seed=B)
 
 
