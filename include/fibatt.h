@@ -23,7 +23,11 @@
  *     [B, H, N].  All tensor pointers are DEVICE pointers owned by the
  *     caller, 16-byte aligned (LSE: 4-byte aligned), on the current device.
  *   - Arithmetic is fp32 with fp32 accumulation; bf16 outputs are rounded to
- *     nearest-even once, at the end.  LSE is the natural log.
+ *     nearest-even once, at the end.  LSE is the natural log.  One exception,
+ *     for bf16 I/O in the shared-memory forward kernels: each softmax weight
+ *     is rounded to bf16 before its P.V update (products exact, sums fp32),
+ *     and O is divided by the sum of those rounded weights, so O stays a
+ *     convex combination of value rows; the LSE uses the fp32 weights.
  *   - fwd/bwd are asynchronous on `stream` and never synchronise.  They do not
  *     allocate device memory.
  *   - A support handle is host memory only (its tables travel to the GPU as

@@ -394,8 +394,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         }
         return;
     }
-    // Consumers.  Use k of stage s is the CTA's unit i = s + k * stages, taken
-    // by group i % groups.  An mbarrier parity wait cannot tell a phase that
+    // Consumers.  Use k of stage s is the CTA's slot i = s + k * stages (its
+    // unit from fwd_slot_unit), taken by group i % groups.  An mbarrier parity wait cannot tell a phase that
     // completed from one two phases ahead, so before waiting for use k to be
     // full the group waits for use k - 1 to be released.  That release wait is
     // itself unambiguous when use k - 2 belonged to this group -- true when
