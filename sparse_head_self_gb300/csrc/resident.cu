@@ -395,12 +395,13 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         return;
     }
     // Consumers.  Use k of stage s is the CTA's slot i = s + k * stages (its
-    // unit from fwd_slot_unit), taken by group i % groups.  An mbarrier parity wait cannot tell a phase that
-    // completed from one two phases ahead, so before waiting for use k to be
-    // full the group waits for use k - 1 to be released.  That release wait is
-    // itself unambiguous when use k - 2 belonged to this group -- true when
-    // groups <= 2, or when stages is a multiple of groups (each stage then
-    // always serves the same group) -- the plan allows nothing else.
+    // unit from fwd_slot_unit), taken by group i % groups.  An mbarrier
+    // parity wait cannot tell a phase that completed from one two phases
+    // ahead, so before waiting for use k to be full the group waits for use
+    // k - 1 to be released.  That release wait is itself unambiguous when use
+    // k - 2 belonged to this group -- true when groups <= 2, or when stages is
+    // a multiple of groups (each stage then always serves the same group) --
+    // the plan allows nothing else.
     const int cw = warp - 1;
     const int grp = cw / p.gwarps, wg = cw % p.gwarps;
     if (grp >= p.groups) return;
