@@ -136,9 +136,10 @@ def test_resident_last_wave_pieces(split, snake, monkeypatch):
     _fwd_full(wl, seed=13)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("pieces", ["0", "1", "1-serial"])
 @pytest.mark.parametrize("B", [13, 14, 27])
-def test_resident_bwd_last_wave_pieces(B, pieces, monkeypatch):
+def test_resident_bwd_last_wave_pieces(B, pieces, dtype, monkeypatch):
     # 156, 168 or 324 heads on (at most) 152 CTAs: the 4, 16 or 20 heads of
     # the partial last wave are cut into pieces of one or two rounds, each
     # piece recomputing P and dS for its key rows (B = 27: two full waves, the
@@ -148,7 +149,8 @@ def test_resident_bwd_last_wave_pieces(B, pieces, monkeypatch):
     monkeypatch.setenv("FIBATT_PATH", "resident")
     monkeypatch.setenv("FIBATT_BWD_PIECES", pieces[0])
     monkeypatch.setenv("FIBATT_BWD_PIECE_PAR", "0" if pieces.endswith("serial") else "1")
-    _bwd_full(WORKLOADS["vitb"].with_batch(B), seed=B)
+    # fp32 rows: four lanes per row, 25 rounds of 8 rows, one stage
+    _bwd_full(Workload(**{**WORKLOADS["vitb"].__dict__, "B": B, "dtype": dtype}), seed=B)
 
 
 @pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
