@@ -171,7 +171,7 @@ std::string tuning_env() {
     std::string r;
     for (const char *n : {"FIBATT_QSPLIT", "FIBATT_LANES", "FIBATT_GROUPS", "FIBATT_STAGES", "FIBATT_BWD_THREADS",
                           "FIBATT_UNROLL", "FIBATT_FWD_THREADS", "FIBATT_PREFETCH", "FIBATT_BWD_LANES", "FIBATT_SPLIT_TAIL",
-                          "FIBATT_BWD_PIECES", "FIBATT_BWD_PIECE_PAR"}) {
+                          "FIBATT_BWD_PIECES", "FIBATT_BWD_PIECE_PAR", "FIBATT_GT_FUSE"}) {
         const char *e = std::getenv(n);
         r += e ? e : "-";
         r += ',';
@@ -369,18 +369,22 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     const PathSel sel = path_sel();
     ResidentPlan pl;
     cudaError_t e;
+    long row0_from = 0;   // global first token: heads from here on get row 0 from the row kernel
     if (s->impl.tab.global0 && sel == PathSel::Generic)
         return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=generic has no global first token");
     if (sel == PathSel::Generic) {
         e = launch_fwd_generic(a);
     } else if (sel != PathSel::Flat && cached_plan(s, false, s->impl.tab, B, dtype, &pl)) {
         e = launch_fwd_resident(a, pl);
+        // fused: the whole-head units wrote row 0; the last wave's pieces did not
+        if (s->impl.tab.global0 && pl.fuse_row0) row0_from = pl.n_keep;
     } else {
         if (sel == PathSel::Resident)
             return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: windows do not fit in shared memory");
         e = launch_fwd_flat(a);
     }
-    if (e == cudaSuccess && s->impl.tab.global0) e = launch_fwd_global_row(a);
+    if (e == cudaSuccess && s->impl.tab.global0 && row0_from < (long)B * s->impl.tab.H)
+        e = launch_fwd_global_row(a, row0_from);
     if (e != cudaSuccess) return cuda_error(e, "fibatt_fwd launch");
     return FIBATT_OK;
 }

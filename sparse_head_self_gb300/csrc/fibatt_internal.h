@@ -96,6 +96,7 @@ struct ResidentPlan {
     int sub_rows;        // forward: query rows per piece; backward: rounds per piece
     size_t split_off;    // backward: byte offset of the pieces' (P, dS) areas
     int piece_par;       // backward: one-round pieces spread over more warps
+    int fuse_row0;       // forward, global first token: row 0 computed inside each whole-head unit
     size_t stage_bytes;  // bytes per ring stage
     size_t smem;         // dynamic shared memory bytes
     int threads;         // threads per CTA (producer warp + consumers)
@@ -144,7 +145,8 @@ cudaError_t read_device_error(unsigned *code, bool clear);
 // Global first token (global_token.cu): the dense row of token 0 (forward,
 // after the banded kernel), its dense row before the banded backward, and
 // the column of key 0 after it.
-cudaError_t launch_fwd_global_row(const FwdArgs &a);
+// Rows 0 of heads bh0 .. B H - 1 (every head when bh0 = 0).
+cudaError_t launch_fwd_global_row(const FwdArgs &a, long bh0 = 0);
 cudaError_t launch_bwd_global_row(const BwdArgs &a);
 cudaError_t launch_bwd_global_col(const BwdArgs &a);
 

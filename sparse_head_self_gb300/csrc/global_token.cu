@@ -75,14 +75,15 @@ __device__ __forceinline__ void merge_warps(float m, float l, float2 acc, float 
 
 template <typename T, int NW>
 __global__ void __launch_bounds__(NW * 32)
-fwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
+fwd_global_row_kernel(int N, long bh0, const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                       float scale_log2, T *__restrict__ O, float *__restrict__ LSE) {
     __shared__ float s_m[NW], s_l[NW];
     __shared__ float2 s_acc[NW * 32];
     grid_dep_wait();
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t base = (size_t)blockIdx.x * N * kHeadDim;
+    const size_t bh = (size_t)bh0 + blockIdx.x;
+    const size_t base = bh * N * kHeadDim;
     const float2 q = row_pair(Q + base, lane);
     float m = -INFINITY, l = 0.f;
     float2 acc = make_float2(0.f, 0.f);
@@ -123,7 +124,7 @@ fwd_global_row_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
     merge_warps<NW>(m, l, acc, s_m, s_l, s_acc, warp, lane, &o, &lse2);
     if (warp == 0) {
         store_pair(O + base, lane, o);
-        if (lane == 0) LSE[(size_t)blockIdx.x * N] = lse2 * kLn2;
+        if (lane == 0) LSE[bh * N] = lse2 * kLn2;
     }
 }
 
@@ -232,10 +233,10 @@ bwd_global_col_kernel(int N, const T *__restrict__ Q, const T *__restrict__ K, c
 }
 
 template <typename T, int NW>
-cudaError_t fwd_global(const FwdArgs &a) {
+cudaError_t fwd_global(const FwdArgs &a, long bh0) {
     const TableArg &tab = *a.tab;
-    const cudaError_t e = launch_kernel(fwd_global_row_kernel<T, NW>, dim3((unsigned)(a.B * tab.H)),
-                                        dim3(NW * 32), 0, a.stream, pdl_enabled(), (int)tab.N,
+    const cudaError_t e = launch_kernel(fwd_global_row_kernel<T, NW>, dim3((unsigned)((long)a.B * tab.H - bh0)),
+                                        dim3(NW * 32), 0, a.stream, pdl_enabled(), (int)tab.N, bh0,
                                         static_cast<const T *>(a.Q), static_cast<const T *>(a.K),
                                         static_cast<const T *>(a.V), a.scale * kLog2e, static_cast<T *>(a.O),
                                         a.LSE);
@@ -267,10 +268,10 @@ cudaError_t bwd_global(const BwdArgs &a, bool row) {
 // 8 warps while a block's rows fit in a few steps, 32 beyond
 constexpr int kGtShortN = 8 * kGtRows * 8;
 
-cudaError_t launch_fwd_global_row(const FwdArgs &a) {
+cudaError_t launch_fwd_global_row(const FwdArgs &a, long bh0) {
     const bool wide = a.tab->N > kGtShortN;
-    if (a.dtype == FIBATT_F32) return wide ? fwd_global<float, 32>(a) : fwd_global<float, 8>(a);
-    return wide ? fwd_global<__nv_bfloat16, 32>(a) : fwd_global<__nv_bfloat16, 8>(a);
+    if (a.dtype == FIBATT_F32) return wide ? fwd_global<float, 32>(a, bh0) : fwd_global<float, 8>(a, bh0);
+    return wide ? fwd_global<__nv_bfloat16, 32>(a, bh0) : fwd_global<__nv_bfloat16, 8>(a, bh0);
 }
 
 static cudaError_t bwd_global_any(const BwdArgs &a, bool row) {

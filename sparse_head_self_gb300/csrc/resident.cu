@@ -65,7 +65,127 @@ struct PipeParams {
     int sub_rows;
     int early_prefetch;   // L2-prefetch the first units before the grid-dependency wait
     int snake;            // odd full waves take the CTAs in reverse order
+    int fuse_row0;        // global first token: row 0 of each whole-head unit computed here
 };
+
+// Row 0 of a whole-head unit with the global first token: query 0 attends
+// every key.  Consumer warp wg of the group takes batches of 16 keys
+// (keys wg 16 + i 16 gwarps ...): two lanes per key score it (half the
+// dims each, 16-byte chunks in an order rotated by key and half, so a
+// quarter warp hits eight distinct bank groups), the batch enters the
+// warp's running softmax state, and every lane then adds the batch's
+// weighted value rows for its two dims.  The warp leaves its state in the
+// stage's partial slot (pacc: gwarps x 32 float2, pm and pl: gwarps floats)
+// and counts itself in; the warp that arrives last merges the states, writes
+// O_0 and LSE_0 and resets the count.  No warp waits for another.  The slot
+// is the stage's own: it is used again only by the stage's next unit, whose
+// data arrives after every consumer warp, the merging one included, has
+// released the stage.
+template <typename T>
+__device__ __forceinline__ void fused_row0(const uint8_t *sQ, const uint8_t *sK, ptrdiff_t vdelta, int N, int wg,
+                                           int gwarps, float sl2, float2 *pacc, float *pm, float *pl, int *count,
+                                           T *O0, float *LSE0) {
+    constexpr bool F32 = std::is_same<T, float>::value;
+    constexpr int RB = (int)sizeof(T) * kHeadDim;
+    constexpr int HC = RB / 32;   // 16-byte chunks in half a row
+    const int lane = threadIdx.x & 31, kl = lane >> 1, half = lane & 1;
+    auto vpair = [&](int k) {
+        const uint8_t *row = sK + vdelta + (size_t)k * RB;
+        if constexpr (F32) {
+            return reinterpret_cast<const float2 *>(row)[lane];
+        } else {
+            const uint32_t w = reinterpret_cast<const uint32_t *>(row)[lane];
+            return make_float2(bf16_lo(w), bf16_hi(w));
+        }
+    };
+    float m = -INFINITY, l = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    for (int kb = wg * 16; kb < N; kb += 16 * gwarps) {
+        const int k = kb + kl;
+        float xa = 0.f, xb = 0.f;
+        if (k < N) {
+            const uint8_t *kr = sK + (size_t)k * RB;
+#pragma unroll
+            for (int c = 0; c < HC; ++c) {
+                const int cc = half * HC + ((c + kl + 4 * half) & (HC - 1));
+                const uint4 qv = *reinterpret_cast<const uint4 *>(sQ + cc * 16);
+                const uint4 kv = *reinterpret_cast<const uint4 *>(kr + cc * 16);
+                if constexpr (F32) {
+                    xa = fmaf(__uint_as_float(qv.x), __uint_as_float(kv.x), xa);
+                    xb = fmaf(__uint_as_float(qv.y), __uint_as_float(kv.y), xb);
+                    xa = fmaf(__uint_as_float(qv.z), __uint_as_float(kv.z), xa);
+                    xb = fmaf(__uint_as_float(qv.w), __uint_as_float(kv.w), xb);
+                } else {
+                    const uint32_t q4[4] = {qv.x, qv.y, qv.z, qv.w}, k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        xa = fmaf(bf16_lo(q4[i]), bf16_lo(k4[i]), xa);
+                        xb = fmaf(bf16_hi(q4[i]), bf16_hi(k4[i]), xb);
+                    }
+                }
+            }
+        }
+        float x = xa + xb;
+        x += __shfl_xor_sync(kFullMask, x, 1);
+        x = k < N ? x * sl2 : -INFINITY;
+        float mb = x;
+#pragma unroll
+        for (int o = 2; o <= 16; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFullMask, mb, o));
+        const float mn = fmaxf(m, mb);   // finite: key kb < N is in the batch
+        const float f = fast_exp2(m - mn);
+        const float pw = fast_exp2(x - mn);
+        float ps = pw;
+#pragma unroll
+        for (int o = 2; o <= 16; o <<= 1) ps += __shfl_xor_sync(kFullMask, ps, o);
+        l = fmaf(l, f, ps);
+        acc.x *= f;
+        acc.y *= f;
+        m = mn;
+        // keys past N have weight 0 and read row N - 1 (finite data)
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const float pt = __shfl_sync(kFullMask, pw, 2 * t);
+            const float2 vv = vpair(min(kb + t, N - 1));
+            acc.x = fmaf(pt, vv.x, acc.x);
+            acc.y = fmaf(pt, vv.y, acc.y);
+        }
+    }
+    if (lane == 0) {
+        pm[wg] = m;
+        pl[wg] = l;
+    }
+    pacc[wg * 32 + lane] = acc;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(count, 1) == gwarps - 1;
+    }
+    if (!__shfl_sync(kFullMask, last, 0)) return;
+    __threadfence_block();
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int w = 0; w < gwarps; ++w) M = fmaxf(M, pm[w]);
+    float L = 0.f;
+    float2 A = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int w = 0; w < gwarps; ++w) {
+        const float fw = pl[w] > 0.f ? fast_exp2(pm[w] - M) : 0.f;
+        L = fmaf(fw, pl[w], L);
+        A.x = fmaf(fw, pacc[w * 32 + lane].x, A.x);
+        A.y = fmaf(fw, pacc[w * 32 + lane].y, A.y);
+    }
+    const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
+    if constexpr (F32) {
+        reinterpret_cast<float2 *>(O0)[lane] = make_float2(A.x * inv, A.y * inv);
+    } else {
+        reinterpret_cast<uint32_t *>(O0)[lane] = pack_bf16x2(A.x * inv, A.y * inv);
+    }
+    if (lane == 0) {
+        *LSE0 = L > 0.f ? (M + fast_log2(L)) * kLn2 : -INFINITY;
+        *count = 0;
+    }
+}
 
 // Unit of this CTA's slot k (-1 past the end).  Slot k of CTA c is wave k,
 // position c; with `snake`, odd full waves run the positions backwards, so a
@@ -84,7 +204,10 @@ struct Unit {
     int bh, h, q0, q1, t0, t1, lo, nrows;
 };
 
-__device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const PipeParams &p, int u) {
+// Geometry of unit u; start and off are the table's head starts and offsets
+// (the kernel parameter's, or a shared-memory copy of them).
+__device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const int *start, const int *off,
+                                              const PipeParams &p, int u) {
     Unit g;
     if (u < p.n_keep) {
         g.bh = u / p.qsplit;
@@ -98,13 +221,13 @@ __device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const PipePar
         g.q1 = min(ce, g.q0 + p.sub_rows);
     }
     g.h = g.bh % tab.H;
-    g.t0 = tab.start[g.h];
-    g.t1 = tab.start[g.h + 1];
+    g.t0 = start[g.h];
+    g.t1 = start[g.h + 1];
     g.lo = 0;
     g.nrows = 0;
     if (g.t1 > g.t0 && g.q1 > g.q0) {
-        g.lo = max(0, g.q0 + tab.off[g.t0]);
-        g.nrows = max(0, min(tab.N, g.q1 + tab.off[g.t1 - 1]) - g.lo);
+        g.lo = max(0, g.q0 + off[g.t0]);
+        g.nrows = max(0, min(tab.N, g.q1 + off[g.t1 - 1]) - g.lo);
     }
     return g;
 }
@@ -286,8 +409,15 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
     fwd_offsets<T, G, UNROLL, W16>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
     if constexpr (GT) {
         // global first token: key 0 for every query row j >= 1 whose band
-        // misses it (offset -j absent; the tables are symmetric)
-        const bool need = valid && j >= 1 && !table_has(off, g.t0, g.t1, j);
+        // misses it (offset -j absent).  The warp marks the round's rows
+        // [jfirst, jlast] that some offset -j reaches, one bit per row,
+        // scanning the head's table 32 entries at a time.
+        unsigned band0 = 0;
+        for (int t = g.t0; t < g.t1; t += 32) {
+            const int o = t + lane < g.t1 ? -off[t + lane] : -1;
+            band0 |= __reduce_or_sync(kFullMask, o >= jfirst && o <= jlast ? 1u << (o - jfirst) : 0u);
+        }
+        const bool need = valid && j >= 1 && !((band0 >> (j - jfirst)) & 1u);
         S kr;
         kr.load(sK0, lg.c);
         float s0 = group_sum<G>(q.dot(kr)) * p.scale_log2;
@@ -297,7 +427,7 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
         kr.load(sV0, lg.c);
         softmax_accumulate<T, G, W16>(st, kr, pr);
     }
-    if (valid) {
+    if (valid && !(GT && p.fuse_row0 && j == 0)) {   // fused: row 0 is written by fused_row0
         const float ln = softmax_norm<T, G, W16>(st);
         const float inv = ln > 0.f ? __frcp_rn(ln) : 0.f;
 #pragma unroll
@@ -311,7 +441,7 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
 template <typename T>
 __device__ __forceinline__ void prefetch_unit(const TableArg &tab, const PipeParams &p, int u) {
     constexpr int RB = sizeof(T) * kHeadDim;
-    const Unit g = unit_geometry(tab, p, u);
+    const Unit g = unit_geometry(tab, tab.start, tab.off, p, u);
     const size_t row0 = (size_t)g.bh * tab.N;
     if (g.q1 > g.q0)
         bulk_prefetch_l2(static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, (uint32_t)(g.q1 - g.q0) * RB);
@@ -330,6 +460,9 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     __shared__ int s_off[kMaxEntries];
+    __shared__ int s_row0_count[kMaxStages];   // fused row 0: warps done with the stage's unit
+    __shared__ Unit s_unit[kMaxStages];        // geometry of the stage's unit, written by the producer
+    __shared__ int s_start[kMaxHeads + 1];     // the heads' table starts
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0 && p.early_prefetch) {
@@ -343,10 +476,12 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         }
     }
     for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
+    for (int t = threadIdx.x; t <= tab.H; t += blockDim.x) s_start[t] = tab.start[t];
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], p.gwarps);
+            s_row0_count[s] = 0;
         }
     }
     __syncthreads();
@@ -371,11 +506,14 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
                     const int un = fwd_slot_unit(p, d);
                     if (un >= 0) prefetch_unit<T>(tab, p, un);
                 }
+            const Unit g = unit_geometry(tab, s_start, s_off, p, u);   // before the wait: off the critical path
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
-            const Unit g = unit_geometry(tab, p, u);
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)g.bh * tab.N;
             const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
+            // the consumers read the geometry after the full phase, which
+            // this arrive (a release) belongs to
+            s_unit[s] = g;
             mbar_expect_tx(&full_bar[s], qb + 2 * kvb + (GT ? 2u * RB : 0u));
             if (qb)   // a last-wave piece past the end of its chunk has no rows
                 bulk_g2s(st + q_off, static_cast<const T *>(p.Q) + (row0 + g.q0) * kHeadDim, qb, &full_bar[s]);
@@ -413,8 +551,21 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const int s = i % p.stages, k = i / p.stages;
         if (k >= 1 && !mbar_wait(&empty_bar[s], (k - 1) & 1)) return;
         if (!mbar_wait(&full_bar[s], k & 1)) return;
-        const Unit g = unit_geometry(tab, p, u);
+        const Unit g = s_unit[s];
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
+        if constexpr (GT) {
+            if (p.fuse_row0 && g.q0 == 0 && g.q1 == tab.N && g.lo == 0 && g.nrows == tab.N) {
+                // stage s's partial slot, after the stages: gwarps x 32
+                // float2 partial accumulators, then gwarps maxima and sums
+                const size_t row0 = (size_t)g.bh * tab.N;
+                float2 *pacc = reinterpret_cast<float2 *>(smem + (size_t)p.stages * p.stage_bytes) +
+                               (size_t)s * p.gwarps * 33;
+                float *pm = reinterpret_cast<float *>(pacc + 32 * p.gwarps);
+                fused_row0<T>(st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), tab.N, wg, p.gwarps,
+                              p.scale_log2, pacc, pm, pm + p.gwarps, &s_row0_count[s],
+                              static_cast<T *>(p.O) + row0 * kHeadDim, p.LSE + row0);
+            }
+        }
         for (int r = wg; r < rpu; r += p.gwarps)
             fwd_round<T, G, UNROLL, GT, true>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
                                     st + g0_off, st + g0_off + RB);
@@ -760,6 +911,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full_bar[2], empty_bar[2], aux_bar[2];
     __shared__ int s_off[kMaxEntries];
+    __shared__ int s_start[kMaxHeads + 1];   // the heads' table starts (per-unit reads from shared memory)
 
     const int N = tab.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -777,6 +929,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         }
     }
     for (int t = threadIdx.x; t < tab.start[tab.H]; t += blockDim.x) s_off[t] = tab.off[t];
+    for (int t = threadIdx.x; t <= tab.H; t += blockDim.x) s_start[t] = tab.start[t];
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -871,7 +1024,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         const int u = bwd_item_unit(p, it);
         const bool piece = !GT && it >= p.n_keep;   // the plan splits no unit with the global token
         const int h = u % tab.H;
-        const int t0 = tab.start[h], t1 = tab.start[h + 1];
+        const int t0 = s_start[h], t1 = s_start[h + 1];
         const size_t row0 = (size_t)u * N;
         if (i == 0) {
             // D_j = <dO_j, O_j> and LSE_j (log2 units), one row per consumer
@@ -1253,10 +1406,10 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     if (const char *e = getenv("FIBATT_UNROLL")) unroll = atoi(e) == 1 ? 1 : 2;
     if (const char *e = getenv("FIBATT_FWD_THREADS")) maxt = atoi(e) == 768 ? 768 : (atoi(e) == 512 ? 512 : 1024);
     if (G == 4) maxt = 1024;
-    if (tab.global0) {   // the global-token kernels exist in the default shape only
+    if (tab.global0) {   // the global-token kernels exist in the two-lane, 512-thread shape only
         G = 2;
-        unroll = 2;
         maxt = 512;
+        if (!getenv("FIBATT_UNROLL")) unroll = 2;
     }
     const int R = 32 / G;                                  // rows per warp round
     const int maxw = maxt / 32;
@@ -1316,18 +1469,36 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->groups = groups;
     pl->gwarps = gwarps;
     pl->stage_bytes = stage;
-    pl->smem = stage * stages;
     pl->threads = 32 * (1 + groups * gwarps);
     const long units = (long)B * tab.H * qsplit;
     pl->grid = (int)std::min<long>(units, sms);
+    const long left = units > pl->grid ? units % pl->grid : 0;   // units of the last, partial wave
+    // With the global first token and whole-head units, row 0 of every head
+    // is computed inside its unit (fused_row0).  That needs every head's
+    // table non-empty (so that its unit stages all N key rows) and room for a
+    // partial-state slot per stage; and it keeps the last wave's units whole,
+    // so it is taken when that wave is empty or at least a quarter full (a
+    // few whole units in a last wave cost more than the separate row kernel
+    // with last-wave pieces).
+    bool staged_all = true;
+    for (int h = 0; h < tab.H; ++h) staged_all = staged_all && tab.start[h + 1] > tab.start[h];
+    pl->fuse_row0 = tab.global0 && qsplit == 1 && staged_all;
+    if (const char *e = getenv("FIBATT_GT_FUSE"))   // 0: never, else whenever possible
+        pl->fuse_row0 = pl->fuse_row0 && atoi(e) != 0;
+    else
+        pl->fuse_row0 = pl->fuse_row0 && (left == 0 || 4 * left >= pl->grid);
+    const size_t slot_bytes = (size_t)gwarps * 33 * sizeof(float2);   // one partial slot per stage
+    if (pl->fuse_row0)
+        while (stages > 2 && (stage + slot_bytes) * stages > budget) pl->stages = --stages;
+    if (pl->fuse_row0 && (stage + slot_bytes) * stages > budget) pl->fuse_row0 = 0;
+    pl->smem = (stage + (pl->fuse_row0 ? slot_bytes : 0)) * stages;
     // cut the units of the last, partial wave into single rounds (at most as
     // many pieces as there are CTAs)
     pl->n_keep = (int)units;
     pl->qsub = 1;
     pl->sub_rows = chunk;
-    const long left = units > pl->grid ? units % pl->grid : 0;
     const char *st = getenv("FIBATT_SPLIT_TAIL");
-    if (left > 0 && !(st && atoi(st) == 0)) {
+    if (left > 0 && !(st && atoi(st) == 0) && !pl->fuse_row0) {
         const int qsub = (int)std::max<long>(1, std::min<long>(chunk / R, pl->grid / left));
         if (qsub > 1) {
             pl->n_keep = (int)(units - left);
@@ -1354,7 +1525,7 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
                  pl.n_keep + (n_reg - pl.n_keep) * pl.qsub, pl.stages, pl.groups, pl.gwarps,
                  (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows, early_prefetch(),
-                 fwd_snake()};
+                 fwd_snake(), pl.fuse_row0};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
@@ -1364,7 +1535,9 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
 template <typename T>
 static cudaError_t fwd_resident_dispatch(const FwdArgs &a, const ResidentPlan &pl) {
     if (a.tab->global0)   // the plan keeps the default shapes for it
-        return pl.lanes == 4 ? fwd_resident<T, 4, 2, 1024, true>(a, pl) : fwd_resident<T, 2, 2, 512, true>(a, pl);
+        return pl.lanes == 4 ? fwd_resident<T, 4, 2, 1024, true>(a, pl)
+                             : (pl.unroll == 2 ? fwd_resident<T, 2, 2, 512, true>(a, pl)
+                                               : fwd_resident<T, 2, 1, 512, true>(a, pl));
     if (pl.lanes == 4) return pl.unroll == 2 ? fwd_resident<T, 4, 2, 1024>(a, pl) : fwd_resident<T, 4, 1, 1024>(a, pl);
     if (pl.maxt == 768) return pl.unroll == 2 ? fwd_resident<T, 2, 2, 768>(a, pl) : fwd_resident<T, 2, 1, 768>(a, pl);
     return pl.unroll == 2 ? fwd_resident<T, 2, 2, 512>(a, pl) : fwd_resident<T, 2, 1, 512>(a, pl);

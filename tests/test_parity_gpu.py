@@ -339,6 +339,32 @@ def test_global_token_edge_sizes(N, kernel_path):
     _global_fwd_bwd(wl, 23)
 
 
+@pytest.mark.parametrize("fuse", ["1", "0", None])
+@pytest.mark.parametrize("name,dtype,B", [("vitb", "bf16", 13), ("vitb", "f32", 13), ("vitb_nodiag", "bf16", 13),
+                                          ("vitb", "bf16", 38)])
+def test_global_token_whole_heads(name, dtype, B, fuse, monkeypatch):
+    # B H >= the SM count: whole-head units, where row 0 is computed inside
+    # the resident forward (fuse 1; by default when the last wave is empty or
+    # at least a quarter full, as for B = 38) or by the dense row kernel
+    # (fuse 0; by default for B = 13, whose last wave has 4 units)
+    monkeypatch.delenv("FIBATT_PATH", raising=False)
+    if fuse is None:
+        monkeypatch.delenv("FIBATT_GT_FUSE", raising=False)
+    else:
+        monkeypatch.setenv("FIBATT_GT_FUSE", fuse)
+    _global_fwd_bwd(Workload(**{**WORKLOADS[name].__dict__, "B": B, "dtype": dtype}), 25)
+
+
+@pytest.mark.parametrize("fuse", ["1", "0"])
+@pytest.mark.parametrize("N", [1, 2, 9, 40])
+def test_global_token_whole_heads_edge_sizes(N, fuse, monkeypatch):
+    # short heads, 180 of them: many stages; N = 1 has empty tables (no
+    # fusion then, the row kernel writes row 0)
+    monkeypatch.delenv("FIBATT_PATH", raising=False)
+    monkeypatch.setenv("FIBATT_GT_FUSE", fuse)
+    _global_fwd_bwd(Workload("edge", 60, 3, N, 64, "f32", 1, N, False, True), 26)
+
+
 def test_global_token_video_two_heads():
     wl = WORKLOADS["video"].with_batch(1)
     _global_fwd_bwd(wl, 24, heads_subset=(0, wl.H - 1))
