@@ -455,12 +455,14 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
     }
 
     cudaError_t e = cudaSuccess;
-    if (a.gw) e = launch_bwd_global_row(a);   // dQ_0 and the weights of the pairs (0, k)
+    // the resident kernel computes the dense row and column itself when the plan fuses them
+    const bool dense_kernels = a.gw && !(path == BwdPath::Resident && pl.fuse_row0);
+    if (dense_kernels) e = launch_bwd_global_row(a);   // dQ_0 and the weights of the pairs (0, k)
     if (e == cudaSuccess)
         e = path == BwdPath::Resident ? launch_bwd_resident(a, pl)
             : path == BwdPath::Flat   ? launch_bwd_flat(a)
                                       : launch_bwd_generic(a);
-    if (e == cudaSuccess && a.gw) e = launch_bwd_global_col(a);   // dK_0, dV_0
+    if (e == cudaSuccess && dense_kernels) e = launch_bwd_global_col(a);   // dK_0, dV_0
     if (e != cudaSuccess) return cuda_error(e, "fibatt_bwd launch");
     return FIBATT_OK;
 }

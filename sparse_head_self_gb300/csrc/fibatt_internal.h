@@ -96,7 +96,9 @@ struct ResidentPlan {
     int sub_rows;        // forward: query rows per piece; backward: rounds per piece
     size_t split_off;    // backward: byte offset of the pieces' (P, dS) areas
     int piece_par;       // backward: one-round pieces spread over more warps
-    int fuse_row0;       // forward, global first token: row 0 computed inside each whole-head unit
+    int fuse_row0;       // global first token: row 0 (forward), row and column 0 (backward) computed inside each
+                         // whole-head unit
+    size_t gt_off;       // backward, fused global token: byte offset of its weights and partial sums
     size_t stage_bytes;  // bytes per ring stage
     size_t smem;         // dynamic shared memory bytes
     int threads;         // threads per CTA (producer warp + consumers)

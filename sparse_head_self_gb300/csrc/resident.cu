@@ -363,16 +363,18 @@ __device__ __forceinline__ void round_range(const int *off, int N, int t0, int t
     te = max(tb, t1 - above);
 }
 
-// Whether the ascending offsets off[t0..t1) contain v (binary search).
-__device__ __forceinline__ bool table_has(const int *off, int t0, int t1, int v) {
-    while (t0 < t1) {
-        const int mid = (t0 + t1) >> 1;
-        const int o = off[mid];
-        if (o == v) return true;
-        if (o < v) t0 = mid + 1;
-        else t1 = mid;
+// Global first token: bit i set when the band of row first + i (i < nrows
+// <= 32) reaches position 0, i.e. offset -(first + i) is in off[t0, t1) (the
+// tables are symmetric, so the same bit says whether +(first + i) is).  The
+// warp scans the head's table 32 entries at a time; call it warp-uniformly.
+__device__ __forceinline__ unsigned band_reaches_zero(const int *off, int t0, int t1, int first, int nrows) {
+    const int lane = threadIdx.x & 31;
+    unsigned hit = 0;
+    for (int t = t0; t < t1; t += 32) {
+        const int i = t + lane < t1 ? -off[t + lane] - first : -1;
+        hit |= __reduce_or_sync(kFullMask, i >= 0 && i < nrows ? 1u << i : 0u);
     }
-    return false;
+    return hit;
 }
 
 // Round r of a unit: query rows [q0 + r R, q0 + r R + R) with R = 32 / G.
@@ -409,14 +411,8 @@ __device__ __forceinline__ void fwd_round(const TableArg &tab, const int *off, c
     fwd_offsets<T, G, UNROLL, W16>(off, N, tb, te, j, valid, g.lo, g.nrows, sK, vdelta, q, lg, p.scale_log2, st);
     if constexpr (GT) {
         // global first token: key 0 for every query row j >= 1 whose band
-        // misses it (offset -j absent).  The warp marks the round's rows
-        // [jfirst, jlast] that some offset -j reaches, one bit per row,
-        // scanning the head's table 32 entries at a time.
-        unsigned band0 = 0;
-        for (int t = g.t0; t < g.t1; t += 32) {
-            const int o = t + lane < g.t1 ? -off[t + lane] : -1;
-            band0 |= __reduce_or_sync(kFullMask, o >= jfirst && o <= jlast ? 1u << (o - jfirst) : 0u);
-        }
+        // misses it
+        const unsigned band0 = band_reaches_zero(off, g.t0, g.t1, jfirst, jlast - jfirst + 1);
         const bool need = valid && j >= 1 && !((band0 >> (j - jfirst)) & 1u);
         S kr;
         kr.load(sK0, lg.c);
@@ -687,7 +683,11 @@ struct BwdParams {
     uint32_t piece_off;   // per phase-B warp of a piece: [max_count][R] (P, dS) pairs
     int snake;            // odd full waves take the CTAs in reverse order (as the forward)
     int piece_par;        // one-round pieces spread over kPieceA + kPieceB warps (see the kernel)
+    int fuse_gt;          // global first token: row 0 and column 0 inside each unit (gt_fused_*)
+    uint32_t gt_off;      // fused global token: byte offset of w0r [2N], w0c [2N], partial sums [3 kGtParts][64]
 };
+
+constexpr int kGtParts = 4;   // fused global token: row ranges per dense sum
 
 constexpr int kPieceA = 3;   // warps on a piece's query round, a third of its offsets each
 constexpr int kPieceB = 6;   // warps on the first pass of its key round, a sixth each
@@ -874,7 +874,10 @@ template <typename T, int G>
 __device__ __forceinline__ void bwd_a_global(const int *off, int t0, int t1, int j, bool valid, const uint8_t *sK0,
                                              ptrdiff_t vdelta, const Slice<T, G> &q, const Slice<T, G> &g, float Dj,
                                              float lse2, float sl2, const LaneGeom<T, G> &lg, float2 (&dq)[32 / G]) {
-    const bool need = valid && j >= 1 && !table_has(off, t0, t1, j);
+    // every lane takes part in the warp-wide scan, whatever its row
+    const int first = __shfl_sync(kFullMask, j, 0);   // the warp's rows are first + lane / G
+    const unsigned hit = band_reaches_zero(off, t0, t1, first, 32 / G);
+    const bool need = valid && j >= 1 && !((hit >> (j - first)) & 1u);
     Slice<T, G> kk, vv;
     kk.load(sK0, lg.c);
     vv.load(sK0 + vdelta, lg.c);
@@ -891,7 +894,10 @@ template <typename T, int G>
 __device__ __forceinline__ void bwd_b_global(const int *off, int t0, int t1, int k, bool valid, const float *gw,
                                              int N, const uint8_t *sQ0, ptrdiff_t gdelta, const LaneGeom<T, G> &lg,
                                              float2 (&dk)[32 / G], float2 (&dv)[32 / G]) {
-    const bool need = valid && k >= 1 && !table_has(off, t0, t1, k);
+    // every lane takes part in the warp-wide scan, whatever its row
+    const int first = __shfl_sync(kFullMask, k, 0);   // the warp's rows are first + lane / G
+    const unsigned hit = band_reaches_zero(off, t0, t1, first, 32 / G);
+    const bool need = valid && k >= 1 && !((hit >> (k - first)) & 1u);
     const float P = need ? gw[k] : 0.f;
     const float dS = need ? gw[N + k] : 0.f;
     Slice<T, G> qq, gg;
@@ -899,6 +905,128 @@ __device__ __forceinline__ void bwd_b_global(const int *off, int t0, int t1, int
     gg.load(sQ0 + gdelta, lg.c);
     qq.axpy(dS, dk);
     gg.axpy(P, dv);
+}
+
+// Half of the dot product of two 64-element rows in shared memory: the
+// lane's half (lane & 1) of the dims, in 16-byte chunks whose order is
+// rotated by rot and the half, so that the eight lanes of a quarter warp (four
+// rows, both halves) read eight distinct bank groups.
+template <typename T>
+__device__ __forceinline__ float half_row_dot(const uint8_t *a, const uint8_t *b, int rot) {
+    constexpr int HC = (int)sizeof(T) * kHeadDim / 32;   // 16-byte chunks in half a row
+    const int half = threadIdx.x & 1;
+    float xa = 0.f, xb = 0.f;
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        const int cc = half * HC + ((c + rot + 4 * half) & (HC - 1));
+        const uint4 x = *reinterpret_cast<const uint4 *>(a + cc * 16);
+        const uint4 y = *reinterpret_cast<const uint4 *>(b + cc * 16);
+        if constexpr (std::is_same<T, float>::value) {
+            xa = fmaf(__uint_as_float(x.x), __uint_as_float(y.x), xa);
+            xb = fmaf(__uint_as_float(x.y), __uint_as_float(y.y), xb);
+            xa = fmaf(__uint_as_float(x.z), __uint_as_float(y.z), xa);
+            xb = fmaf(__uint_as_float(x.w), __uint_as_float(y.w), xb);
+        } else {
+            xa = dot2_bf16(x.x, y.x, xa);
+            xb = dot2_bf16(x.y, y.y, xb);
+            xa = dot2_bf16(x.z, y.z, xa);
+            xb = dot2_bf16(x.w, y.w, xb);
+        }
+    }
+    return xa + xb;
+}
+
+// Global first token inside a whole-head unit of the backward, phase A: the
+// weights of the dense row 0 (pairs (0, k), every key k) into w0r = [P_0k |
+// dS_0k], and of the dense column 0 (pairs (j, 0), every query j) into w0c =
+// [P_j0 | dS_j0], with P = exp(s - LSE) and dS = P (dP - D) of the row's own
+// query.  Two lanes per row, 16 rows per warp batch.  The stage holds Q, K,
+// V, dO at sQ + {0, 1, 2, 3} tens; sD and sL are D_j and LSE_j (log2 units).
+template <typename T>
+__device__ __forceinline__ void gt_fused_weights(const uint8_t *sQ, size_t tens, const float *sD, const float *sL,
+                                                 int N, int cw, int cwarps, float sl2, float *w0r, float *w0c) {
+    constexpr int RB = (int)sizeof(T) * kHeadDim;
+    const int lane = threadIdx.x & 31, kl = lane >> 1;
+    const uint8_t *sK = sQ + tens, *sV = sQ + 2 * tens, *sG = sQ + 3 * tens;
+    for (int rb = cw * 16; rb < N; rb += 16 * cwarps) {
+        const int r = min(rb + kl, N - 1);   // rows past N repeat row N - 1 and are not stored
+        float s = half_row_dot<T>(sQ, sK + (size_t)r * RB, kl);
+        float dp = half_row_dot<T>(sG, sV + (size_t)r * RB, kl);
+        float sc = half_row_dot<T>(sQ + (size_t)r * RB, sK, kl);
+        float dpc = half_row_dot<T>(sG + (size_t)r * RB, sV, kl);
+        s += __shfl_xor_sync(kFullMask, s, 1);
+        dp += __shfl_xor_sync(kFullMask, dp, 1);
+        sc += __shfl_xor_sync(kFullMask, sc, 1);
+        dpc += __shfl_xor_sync(kFullMask, dpc, 1);
+        if ((lane & 1) == 0 && rb + kl < N) {
+            const float P = fast_exp2(fmaf(s, sl2, -sL[0]));
+            w0r[r] = P;
+            w0r[N + r] = P * (dp - sD[0]);
+            const float Pc = fast_exp2(fmaf(sc, sl2, -sL[r]));
+            w0c[r] = Pc;
+            w0c[N + r] = Pc * (dpc - sD[r]);
+        }
+    }
+}
+
+// Phase B: the three dense sums of the global first token, dQ_0 = scale
+// sum_k dS_0k K_k, dK_0 = scale sum_j dS_j0 Q_j and dV_0 = sum_j P_j0 dO_j.
+// Item = sum x row range (kGtParts ranges); the warp sums its item's rows,
+// two dims per lane, into its partial slot and counts itself in; the warp
+// whose item arrives last adds the partials in a fixed order (so the result
+// does not depend on which warp that is), writes the three rows and resets
+// the count.
+template <typename T>
+__device__ __forceinline__ void gt_fused_sums(const uint8_t *sQ, size_t tens, int N, int item, const float *w0r,
+                                              const float *w0c, float2 *part, int *count, float scale, T *dQ0,
+                                              T *dK0, T *dV0) {
+    constexpr int RB = (int)sizeof(T) * kHeadDim;
+    const int lane = threadIdx.x & 31;
+    const int v = item / kGtParts, q = item % kGtParts;
+    const float *w = v == 0 ? w0r + N : (v == 1 ? w0c + N : w0c);
+    const uint8_t *X = v == 0 ? sQ + tens : (v == 1 ? sQ : sQ + 3 * tens);
+    const int r0 = q * N / kGtParts, r1 = (q + 1) * N / kGtParts;
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+        const float wr = w[r];
+        float2 x;
+        if constexpr (std::is_same<T, float>::value) {
+            x = reinterpret_cast<const float2 *>(X + (size_t)r * RB)[lane];
+        } else {
+            const uint32_t b = reinterpret_cast<const uint32_t *>(X + (size_t)r * RB)[lane];
+            x = make_float2(bf16_lo(b), bf16_hi(b));
+        }
+        acc.x = fmaf(wr, x.x, acc.x);
+        acc.y = fmaf(wr, x.y, acc.y);
+    }
+    part[item * 32 + lane] = acc;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(count, 1) == 3 * kGtParts - 1;
+    }
+    if (!__shfl_sync(kFullMask, last, 0)) return;
+    __threadfence_block();
+#pragma unroll
+    for (int vv = 0; vv < 3; ++vv) {
+        float2 t = part[(vv * kGtParts) * 32 + lane];
+#pragma unroll
+        for (int qq = 1; qq < kGtParts; ++qq) {
+            const float2 y = part[(vv * kGtParts + qq) * 32 + lane];
+            t.x += y.x;
+            t.y += y.y;
+        }
+        const float f = vv == 2 ? 1.f : scale;
+        T *dst = vv == 0 ? dQ0 : (vv == 1 ? dK0 : dV0);
+        if constexpr (std::is_same<T, float>::value) {
+            reinterpret_cast<float2 *>(dst)[lane] = make_float2(t.x * f, t.y * f);
+        } else {
+            reinterpret_cast<uint32_t *>(dst)[lane] = pack_bf16x2(t.x * f, t.y * f);
+        }
+    }
+    if (lane == 0) *count = 0;
 }
 
 // MAXT: threads per CTA the register budget is sized for (65536 / MAXT each).
@@ -912,6 +1040,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     __shared__ uint64_t full_bar[2], empty_bar[2], aux_bar[2];
     __shared__ int s_off[kMaxEntries];
     __shared__ int s_start[kMaxHeads + 1];   // the heads' table starts (per-unit reads from shared memory)
+    __shared__ int s_gt_count;               // fused global token: dense-sum items done in this unit
 
     const int N = tab.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -936,6 +1065,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             mbar_init(&empty_bar[s], 1);
             mbar_init(&aux_bar[s], 1);
         }
+        s_gt_count = 0;
     }
     __syncthreads();
     grid_dep_wait();
@@ -1193,11 +1323,15 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                                 scr, dq);
             if constexpr (GT)
                 bwd_a_global<T, G>(s_off, t0, t1, j, valid, sK, (ptrdiff_t)tens, q, g, Dj, lse2, p.scale_log2, lg, dq);
-            if (valid && !(GT && j == 0)) {   // dQ_0: dense-row kernel
+            if (valid && !(GT && j == 0)) {   // dQ_0: the dense row (fused below or the row kernel)
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
                 S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
             }
+        }
+        float *w0r = reinterpret_cast<float *>(smem + p.gt_off), *w0c = w0r + 2 * N;
+        if constexpr (GT) {
+            if (p.fuse_gt) gt_fused_weights<T>(sQ, tens, sD, sL, N, cw, p.cwarps, p.scale_log2, w0r, w0c);
         }
         consumer_sync(cthreads);
         // ---- phase B: key rows
@@ -1214,13 +1348,22 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             bwd_b_offsets<T, G>(s_off, N, t0, t1, tb, te, k, valid, sQ, (ptrdiff_t)(3 * tens), lg, scr, dk,
                                 dv);
             if constexpr (GT)
-                bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.gw + (size_t)u * 2 * N, N, sQ, (ptrdiff_t)(3 * tens),
-                                   lg, dk, dv);
-            if (valid && !(GT && k == 0)) {   // dK_0, dV_0: column kernel
+                bwd_b_global<T, G>(s_off, t0, t1, k, valid, p.fuse_gt ? w0r : p.gw + (size_t)u * 2 * N, N, sQ,
+                                   (ptrdiff_t)(3 * tens), lg, dk, dv);
+            if (valid && !(GT && k == 0)) {   // dK_0, dV_0: the dense column (fused below or the column kernel)
 #pragma unroll
                 for (int x = 0; x < 32 / G; ++x) dk[x] = mul2(dk[x], make_float2(p.scale, p.scale));
                 S::store(static_cast<T *>(p.dK) + (row0 + k) * kHeadDim, lg.c, dk);
                 S::store(static_cast<T *>(p.dV) + (row0 + k) * kHeadDim, lg.c, dv);
+            }
+        }
+        if constexpr (GT) {
+            if (p.fuse_gt) {
+                float2 *part = reinterpret_cast<float2 *>(w0c + 2 * N);
+                for (int item = cw; item < 3 * kGtParts; item += p.cwarps)
+                    gt_fused_sums<T>(sQ, tens, N, item, w0r, w0c, part, &s_gt_count, p.scale,
+                                     static_cast<T *>(p.dQ) + row0 * kHeadDim, static_cast<T *>(p.dK) + row0 * kHeadDim,
+                                     static_cast<T *>(p.dV) + row0 * kHeadDim);
             }
         }
         consumer_sync(cthreads);   // scratch and stage free for the next unit
@@ -1617,6 +1760,24 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
             }
         }
     }
+    // Global first token: the dense row 0 and column 0 inside each unit
+    // (gt_fused_weights, gt_fused_sums) when their weights and partial sums
+    // fit beside the stages; otherwise the row and column kernels.
+    pl->fuse_row0 = 0;
+    pl->gt_off = 0;
+    if (tab.global0) {
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        const size_t static_smem = 2048 + sizeof(int) * kMaxEntries;   // barriers, starts + offsets, rounded up
+        const size_t gt_bytes = ((4 * (size_t)N + 3 * kGtParts * kHeadDim) * sizeof(float) + 127) / 128 * 128;
+        bool fuse = pl->smem + gt_bytes + static_smem <= (size_t)optin;
+        if (const char *e = getenv("FIBATT_GT_FUSE")) fuse = fuse && atoi(e) != 0;
+        if (fuse) {
+            pl->fuse_row0 = 1;
+            pl->gt_off = pl->smem;
+            pl->smem += gt_bytes;
+        }
+    }
     pl->threads = 32 * (1 + pl->gwarps);
     return true;
 }
@@ -1645,7 +1806,8 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 items, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
                 (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch(),
-                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off, bwd_snake(), pl.piece_par};
+                pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off, bwd_snake(), pl.piece_par,
+                pl.fuse_row0, (uint32_t)pl.gt_off};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
     count_launches(1);
