@@ -120,11 +120,13 @@ fibatt_status fibatt_support_build_distances(int H, int N, const int32_t *counts
  * it, on top of the banded Fibonacci support (Fibottention README,
  * Algorithm 2, whose mask keeps row 0 and column 0 all ones).  The signed
  * tables keep describing the banded part; fibatt_support_get's pair counts
- * include the global pairs.  With it enabled, fibatt_fwd and fibatt_bwd run
- * three extra small kernels (the dense row of token 0, and for the backward
- * its dense row and the column of key 0), FIBATT_PATH=generic and
- * fibatt_bwd_noalloc are UNSUPPORTED, and the backward's workspace grows by
- * 2 x N fp32 per (b, h).  Not thread-safe against calls using the support. */
+ * include the global pairs.  With it enabled, the dense row of token 0 (and
+ * for the backward its dense row and the column of key 0) is computed inside
+ * the shared-memory-resident kernels when their plan allows it, else by up to
+ * three extra small kernels; FIBATT_PATH=generic and fibatt_bwd_noalloc are
+ * UNSUPPORTED, and the backward's workspace grows by 2 x N fp32 per (b, h)
+ * (used by the extra kernels only).  Not thread-safe against calls using the
+ * support. */
 fibatt_status fibatt_support_set_global_token(fibatt_support_t s, int enabled);
 
 /* Sizes of a support: heads, tokens, and total signed entries. */
