@@ -5,14 +5,22 @@ One step = one pass of the whole path over one batch of the workload:
 support build (host), forward (O, LSE) and backward (dQ, dK, dV), through
 the C ABI of libfibatt.  Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload vitb]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+The headline workload is the largest single-GPU configuration (long:
+B=2, H=16, N=16385, fwd+bwd, bf16).  The same line carries, per workload
+(tiny, vitb, vitb_nodiag, video, train, long), the forward and backward
+kernel times, pairs/s, GB/s and the fraction of the binding roofline.
 
 Timing: W untimed steps, then exactly K steps between two CUDA events,
 bracketed by a barrier and torch.cuda.synchronize(); max over ranks.  Inputs
 rotate over enough copies that each step's tensors are evicted from L2 (129
-MB) by the steps in between.  Kernel durations come from CUDA events recorded
-on the launch stream around every fwd and bwd call inside the timed region.
+MB) by the steps in between.  Per-kernel durations come from back-to-back
+loops of one call kind on the same rotating sets (CUDA events at the ends).
+nvidia-smi samples the clocks from the start of the timed region to the end
+of the per-kernel loops.  With --gpus N > 1 and no torchrun environment,
+bench.py starts the N ranks itself (one process per GPU).
 """
 from __future__ import annotations
 
@@ -41,6 +49,8 @@ METRIC = ("attended query-key pairs/sec and achieved HBM GB/s (% of GB300 peak),
           "fwd and fwd+bwd")
 UNIT = "pairs/s"
 FALLBACK_HBM_GBS = 6800.0
+HEADLINE = "long"   # the largest configuration that fits one GPU
+RECORD_WORKLOADS = ("tiny", "vitb", "vitb_nodiag", "video", "train", "long")
 
 
 # ------------------------------------------------------------------ helpers
@@ -51,7 +61,10 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="vitb")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    p.add_argument("--profile-run", action="store_true",
+                   help="warm-up and timed steps of the workload only (no per-workload records, end-to-end "
+                        "run or CPU baseline): the command profiled by ncu")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--block", action="store_true",
@@ -133,8 +146,15 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since it was taken."""
+    """DRAM traffic of one call from the committed ncu record, or None when
+    the kernel sources changed since it was taken.
+
+    Reads are ``dram__bytes_read.sum``.  A kernel's writes mostly end in L2
+    as dirty lines that reach DRAM after the kernel has ended (ncu then
+    counts them nowhere), so the write side is the larger of
+    ``dram__bytes_write.sum`` and the bytes the SMs wrote into L2
+    (``lts__t_sectors_op_write.sum`` x 32 B): every byte written into L2
+    goes to DRAM once.  Returns {"read", "write", "total", ...}."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -142,9 +162,32 @@ def recorded_traffic(kernel: str, workload: str):
         ent = d[workload][kernel]
         if ent.get("source_hash") != kernel_source_hash():
             return None
-        return int(ent["dram_bytes_per_launch"])
+        rd = int(ent["dram_read"])
+        wr = max(int(ent["dram_write"]), int(ent["l2_write"]))
+        out = {"read": rd, "write": wr, "total": rd + wr, "dram_write": int(ent["dram_write"]),
+               "l2_write": int(ent["l2_write"]), "capture": ent.get("capture")}
+        if "scaled_from" in ent:
+            out["scaled_from"] = ent["scaled_from"]
+        return out
     except Exception:
         return None
+
+
+def roofline_record(wl, kind: str, ms: float, pairs: int, hbm_peak: float, peak_kind: str):
+    """Roofline of one call kind ("fwd" or "bwd") of a workload: achieved HBM
+    GB/s (algorithmic bytes over the measured time) and FP32 TFLOP/s (flops
+    per attended pair over the same time), each against its peak, and which
+    of the two roofs binds (the larger ideal time)."""
+    nbytes = algorithmic_bytes(wl, kind == "bwd")
+    flops = pairs * FLOPS_PER_PAIR[kind]
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    t_alu = flops / (FP32_PEAK_TFLOPS * 1e12)
+    gbs = nbytes / ms / 1e6
+    tfl = flops / (ms / 1e3) / 1e12
+    return {"ms": round(ms, 5), "pairs_per_s": pairs / (ms / 1e3), "GB_s": round(gbs, 1),
+            "frac_hbm": round(gbs / hbm_peak, 4), "TFLOP_s": round(tfl, 2),
+            "frac_alu": round(tfl / FP32_PEAK_TFLOPS, 4), "algorithmic_bytes": nbytes, "flops": flops,
+            "bound": "alu" if t_alu > t_hbm else "hbm", "hbm_peak_kind": peak_kind}
 
 
 class ClockSampler:
@@ -254,27 +297,34 @@ class Step:
             ev[2].record()
         L.fibatt_support_destroy(h)
 
-    def kernel_ms(self, rotate: int, stream: int, n: int):
+    def kernel_ms(self, rotate: int, stream: int, n: int = 0, seconds: float = 0.25):
         """Average device time of one forward and of one backward call, each
-        measured over n back-to-back calls on the rotating sets (CUDA events
-        on the launching stream around the whole run)."""
+        measured over back-to-back calls on the rotating sets (CUDA events on
+        the launching stream around the whole run): n calls, or (n = 0) as
+        many as take about `seconds` (at least 20), from a short calibration."""
         L, wl = self.lib, self.wl
         h = ctypes.c_void_p()
         _native.check(L.fibatt_support_build(wl.H, wl.N, self.a, self.b, self.w, int(wl.diag),
                                              ctypes.byref(h)))
         _native.check(L.fibatt_support_set_global_token(h, int(self.global_token)))
-        out = []
+        out, calls = [], []
         for kind in ("fwd", "bwd"):
-            for i in range(3):
-                self._call(kind, h, i % rotate, stream)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
-            for i in range(n):
+            for i in range(5):
                 self._call(kind, h, i % rotate, stream)
             e.record()
             e.synchronize()
-            out.append(s.elapsed_time(e) / n)
+            cnt = n if n > 0 else int(min(20000, max(20, seconds / max(s.elapsed_time(e) / 5e3, 1e-7))))
+            s.record()
+            for i in range(cnt):
+                self._call(kind, h, i % rotate, stream)
+            e.record()
+            e.synchronize()
+            out.append(s.elapsed_time(e) / cnt)
+            calls.append(cnt)
         L.fibatt_support_destroy(h)
+        self.calls = calls
         return out[0], out[1]
 
     def _call(self, kind, h, r, stream):
@@ -380,26 +430,69 @@ def _row_pairs(N, table, global_token, rows):
 
 def cpu_baseline(wl, target_s: float, global_token: bool = False):
     """The fp64 oracle as it stands, on the host cores, on a bounded sample of
-    the workload: forward and backward of whole (b, h) heads, all rows."""
+    the workload: forward and backward of blocks of query/key rows, one head
+    after another (heads 1, 2, ..., each sampled at evenly spread rows), for
+    about target_s seconds.  The unit is attended pairs of the sampled query
+    rows per second (each sampled row's forward, its dQ and the dK, dV of the
+    key row with the same index)."""
     import oracle
     cores = oracle.set_threads(oracle.max_threads())
     q, k, v, do = make_inputs(wl.with_batch(1), 0)
     heads = _oracle_heads(wl, global_token)
-    pairs_head = [oracle.support_size(wl.N, hd) if wl.N <= 2048 else
-                  _row_pairs(wl.N, oracle.signed_table(wl.N, hd), global_token, range(wl.N)) for hd in heads]
-    done_pairs, done_heads, t0 = 0, 0, time.perf_counter()
+    tables = [oracle.signed_table(wl.N, hd) for hd in heads]
+    block = max(1, min(wl.N, 4 * cores))
+    done_pairs, done_rows, t0, i = 0, 0, time.perf_counter(), 0
     while True:
-        h = done_heads % wl.H
-        oracle.fwd_head(q[0, h], k[0, h], v[0, h], heads[h], wl.scale)
-        oracle.bwd_head(q[0, h], k[0, h], v[0, h], do[0, h], heads[h], wl.scale)
-        done_pairs += pairs_head[h]
-        done_heads += 1
+        h = i % wl.H
+        start = (i // wl.H) * 7919 % wl.N   # spread the blocks over the sequence
+        rows = sorted({(start + t * max(1, wl.N // block)) % wl.N for t in range(block)})
+        oracle.fwd_head(q[0, h], k[0, h], v[0, h], heads[h], wl.scale, rows=rows)
+        oracle.bwd_head(q[0, h], k[0, h], v[0, h], do[0, h], heads[h], wl.scale, qrows=rows, krows=rows)
+        done_pairs += _row_pairs(wl.N, tables[h], global_token, rows)
+        done_rows += len(rows)
+        i += 1
         el = time.perf_counter() - t0
-        if el >= target_s or done_heads >= wl.B * wl.H:
+        if el >= target_s or done_rows >= wl.B * wl.H * wl.N:
             break
     return {"value": done_pairs / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"fwd+bwd of {done_heads} of the workload's {wl.B * wl.H} (b,h) heads, "
-                       f"all {wl.N} rows each, fp64, {el:.1f} s")}
+            "sample": (f"fp64 oracle fwd+bwd of {done_rows} query/key rows ({i} blocks of up to {block} rows spread "
+                       f"over heads 1..{min(i, wl.H)} of batch element 0) of the {wl.name} workload, "
+                       f"{done_pairs} attended pairs, {el:.1f} s")}
+
+
+def _rotation(step_probe_bytes: int, l2: int) -> int:
+    """Input/output sets to rotate so that every set is evicted from L2 by
+    the others before it is used again (at most 64 sets)."""
+    return int(min(64, max(2, math.ceil(3 * l2 / step_probe_bytes) + 1)))
+
+
+def _make_step(wl, dev, l2, global_token):
+    probe = Step(wl, dev, 1, global_token=global_token)
+    per_set = probe.bytes_per_set()
+    del probe
+    rotate = _rotation(per_set, l2)
+    return Step(wl, dev, rotate, global_token=global_token), rotate, per_set
+
+
+def workload_record(step, rotate, sptr, hbm_peak, peak_kind, seconds=0.25):
+    """Forward and backward kernel times of one workload (back-to-back loops)
+    and their rooflines."""
+    wl = step.wl
+    fwd_ms, bwd_ms = step.kernel_ms(rotate, sptr, seconds=seconds)
+    fwd = roofline_record(wl, "fwd", fwd_ms, step.pairs, hbm_peak, peak_kind)
+    bwd = roofline_record(wl, "bwd", bwd_ms, step.pairs, hbm_peak, peak_kind)
+    fb, bb = fwd["algorithmic_bytes"], bwd["algorithmic_bytes"]
+    rec = {"B": wl.B, "H": wl.H, "N": wl.N, "dtype": wl.dtype, "diag": wl.diag,
+           "w": [wl.w_min, wl.w_max], "pairs": step.pairs, "fwd": fwd, "bwd": bwd,
+           "fwd_bwd": {"ms": round(fwd_ms + bwd_ms, 5),
+                       "pairs_per_s": step.pairs / ((fwd_ms + bwd_ms) / 1e3),
+                       "GB_s": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6, 1),
+                       "frac_hbm": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6 / hbm_peak, 4)},
+           "calls_timed": {"fwd": step.calls[0], "bwd": step.calls[1]},
+           "l2": f"{rotate} rotating sets"}
+    if wl.name == "tiny":
+        rec["note"] = "launch-bound (0.2 MB per call): parity case, no roofline claim"
+    return rec, fwd_ms, bwd_ms
 
 
 def gb300_arm(args):
@@ -411,11 +504,7 @@ def gb300_arm(args):
     init_dist(world, "nccl")
     wl = WORKLOADS[args.workload]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    probe = Step(wl, dev, 1, global_token=args.global_token)
-    per_set = probe.bytes_per_set()
-    rotate = max(2, math.ceil(3 * l2 / per_set) + 1)
-    del probe
-    step = Step(wl, dev, rotate, global_token=args.global_token)
+    step, rotate, per_set = _make_step(wl, dev, l2, args.global_token)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
@@ -429,7 +518,8 @@ def gb300_arm(args):
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     barrier(world)
     torch.cuda.synchronize(dev)
-    clocks.start()
+    if not args.profile_run:
+        clocks.start()
     launches0 = step.lib.fibatt_launch_count()
     # the timed region: K whole steps back to back (no event between the
     # kernels, so each launch may overlap the previous kernel's drain)
@@ -439,34 +529,52 @@ def gb300_arm(args):
     end.record()
     torch.cuda.synchronize(dev)
     launches = step.lib.fibatt_launch_count() - launches0
-    # per-kernel durations: the same calls, one kind at a time, back to back
-    fwd_ms, bwd_ms = step.kernel_ms(rotate, sptr, min(K, 2000))
+    barrier(world)
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    if args.profile_run:
+        if rank == 0:
+            print(json.dumps({"profile_run": wl.name, "steps": K, "ms_per_step": elapsed_ms / K}), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    t_loops = time.perf_counter()
+    # per-kernel durations of the headline workload, then of every other
+    # workload (each allocated in turn), the clock sampler still running
+    head_rec, fwd_ms, bwd_ms = workload_record(step, rotate, sptr, peak, peak_kind)
+    records = {}
+    for name in RECORD_WORKLOADS:
+        if name == wl.name:
+            records[name] = head_rec
+            continue
+        sub, srot, _ = _make_step(WORKLOADS[name], dev, l2, args.global_token)
+        records[name], _, _ = workload_record(sub, srot, sptr, peak, peak_kind)
+        del sub
+        torch.cuda.empty_cache()
+    loops_s = time.perf_counter() - t_loops
     dev_err = ctypes.c_uint(0)
     _native.check(step.lib.fibatt_device_error(1, ctypes.byref(dev_err)))
     if dev_err.value:
         raise SystemExit(f"device error word set during the timed region: {dev_err.value:#x}")
-    barrier(world)
     clk = clocks.stop()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    if clk is not None:
+        clk["window"] = (f"from the start of the timed region to the end of the per-kernel loops of every "
+                         f"workload ({loops_s:.1f} s)")
 
     ms_step = elapsed_ms / K
     value = whole_job_value(step.pairs, K, world, elapsed_ms)
-    peak, peak_kind = measured_peaks()
-    fb, bb = algorithmic_bytes(wl, False), algorithmic_bytes(wl, True)
-    fwd_gbs, bwd_gbs = fb / fwd_ms / 1e6, bb / bwd_ms / 1e6
     dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
-    d_bytes, d_ms = (bb, bwd_ms) if dominant == "bwd" else (fb, fwd_ms)
+    d = head_rec[dominant]
     kname = f"fibatt_{dominant}"
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(d_bytes / d_ms / 1e6, 1),
-                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(d_bytes / d_ms / 1e6 / peak, 4),
-                "traffic": recorded_traffic(kname, wl.name),
-                "algorithmic_bytes": d_bytes, "avg_ms": round(d_ms, 5)}
-    d_tflops = step.pairs * FLOPS_PER_PAIR[dominant] / (d_ms / 1e3) / 1e12   # one GPU, like the HBM line
-    roofline_alu = {"bound": "alu", "kernel": kname, "achieved": round(d_tflops, 2),
-                    "peak": round(FP32_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
-                    "frac": round(d_tflops / FP32_PEAK_TFLOPS, 4),
-                    "flops_per_pair": FLOPS_PER_PAIR[dominant]}
+    traffic = recorded_traffic(kname, wl.name)
+    hbm_line = {"bound": "hbm", "kernel": kname, "achieved": d["GB_s"], "peak": peak, "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": d["frac_hbm"], "traffic": None if traffic is None else traffic["total"],
+                "traffic_detail": traffic, "algorithmic_bytes": d["algorithmic_bytes"], "avg_ms": d["ms"]}
+    alu_line = {"bound": "alu", "kernel": kname, "achieved": d["TFLOP_s"], "peak": round(FP32_PEAK_TFLOPS, 1),
+                "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz", "unit": "TFLOP/s",
+                "frac": d["frac_alu"], "traffic": None if traffic is None else traffic["total"],
+                "flops_per_pair": FLOPS_PER_PAIR[dominant], "flops": d["flops"], "avg_ms": d["ms"]}
+    roofline, secondary = (alu_line, hbm_line) if d["bound"] == "alu" else (hbm_line, alu_line)
 
     e2e_ms, h2d, d2h = run_e2e(step, dev, args.e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
@@ -484,17 +592,12 @@ def gb300_arm(args):
                    "l2": (f"{rotate} rotating input/output sets of {per_set / 1e6:.0f} MB "
                           f"(> {l2 / 1e6:.0f} MB L2 between reuses)"),
                    "parallelism": f"replicas over B, {world} GPU(s), no collective"},
-        "fwd": {"ms": round(fwd_ms, 5), "pairs_per_s": world * step.pairs / (fwd_ms / 1e3),
-                "GB_s": round(fwd_gbs, 1), "frac_hbm": round(fwd_gbs / peak, 4),
-                "algorithmic_bytes": fb},
-        "bwd": {"ms": round(bwd_ms, 5), "pairs_per_s": world * step.pairs / (bwd_ms / 1e3),
-                "GB_s": round(bwd_gbs, 1), "frac_hbm": round(bwd_gbs / peak, 4),
-                "algorithmic_bytes": bb},
-        "fwd_bwd": {"ms": round(fwd_ms + bwd_ms, 5),
-                    "GB_s": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6, 1),
-                    "frac_hbm": round((fb + bb) / (fwd_ms + bwd_ms) / 1e6 / peak, 4)},
+        "fwd": head_rec["fwd"],
+        "bwd": head_rec["bwd"],
+        "fwd_bwd": head_rec["fwd_bwd"],
         "roofline": roofline,
-        "roofline_alu": roofline_alu,
+        "roofline_secondary": secondary,
+        "workloads": records,
         "e2e": {"value": world * step.pairs / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": args.e2e_steps},
@@ -618,14 +721,52 @@ def block_arm(args):
     print(json.dumps(out), flush=True)
 
 
+def _rank_entry(rank: int, world: int, port: int, target, args):
+    """One rank started by launch_ranks: the torchrun environment, then the arm."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank), LOCAL_WORLD_SIZE=str(world))
+    target(args)
+
+
+def launch_ranks(world: int, target, args) -> None:
+    """Start `world` ranks of `target(args)` as processes on this node (one per
+    GPU, rank r on cuda:r), rendezvous on 127.0.0.1, and wait for all of them;
+    what torchrun would do for `bench.py --gpus N`."""
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_rank_entry, args=(r, world, port, target, args)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    codes = []
+    for pr in procs:
+        pr.join()
+        codes.append(pr.exitcode)
+    if any(c != 0 for c in codes):
+        raise SystemExit(f"bench ranks exited with codes {codes}")
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
-        reference_arm(args)
+        arm = reference_arm
     elif args.block:
-        block_arm(args)
+        arm = block_arm
     else:
-        gb300_arm(args)
+        arm = gb300_arm
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is not None and int(env_world) != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={env_world}: launch one rank per GPU "
+                         f"(torchrun --nproc-per-node {args.gpus}, or no torchrun at all)")
+    if env_world is None and args.gpus > 1:
+        if arm is block_arm:
+            raise SystemExit("--block runs on one GPU")
+        launch_ranks(args.gpus, arm, args)
+        return
+    arm(args)
 
 
 if __name__ == "__main__":

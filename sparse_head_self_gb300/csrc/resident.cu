@@ -459,6 +459,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     __shared__ int s_row0_count[kMaxStages];   // fused row 0: warps done with the stage's unit
     __shared__ Unit s_unit[kMaxStages];        // geometry of the stage's unit, written by the producer
     __shared__ int s_start[kMaxHeads + 1];     // the heads' table starts
+    __shared__ int s_abort;                    // a bounded wait of this CTA gave up (mbar_wait)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0 && p.early_prefetch) {
@@ -479,6 +480,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
             mbar_init(&empty_bar[s], p.gwarps);
             s_row0_count[s] = 0;
         }
+        s_abort = 0;
     }
     __syncthreads();
     // touch no global memory before the previous kernel has completed; then
@@ -493,6 +495,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         // producer: one lane streams every unit of this CTA into the ring and
         // keeps the next `prefetch` units warming in L2
         if (lane != 0) return;
+        int issued = 0;   // units whose copies this lane issued (stage i % stages, use i / stages)
         for (int i = 0;; ++i) {
             const int u = fwd_slot_unit(p, i);
             if (u < 0) break;
@@ -503,7 +506,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
                     if (un >= 0) prefetch_unit<T>(tab, p, un);
                 }
             const Unit g = unit_geometry(tab, s_start, s_off, p, u);   // before the wait: off the critical path
-            if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
+            if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1, &s_abort)) break;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)g.bh * tab.N;
             const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
@@ -521,11 +524,15 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
                 bulk_g2s(st + g0_off, static_cast<const T *>(p.K) + row0 * kHeadDim, RB, &full_bar[s]);
                 bulk_g2s(st + g0_off + RB, static_cast<const T *>(p.V) + row0 * kHeadDim, RB, &full_bar[s]);
             }
+            issued = i + 1;
             if (i >= 1 && p.prefetch > 0) {
                 const int un = fwd_slot_unit(p, i + p.stages + p.prefetch - 1);
                 if (un >= 0) prefetch_unit<T>(tab, p, un);
             }
         }
+        // leave only once the last copies into every stage have landed
+        for (int s = 0; s < p.stages && s < issued; ++s)
+            mbar_drain(&full_bar[s], ((issued - 1 - s) / p.stages) & 1);
         return;
     }
     // Consumers.  Use k of stage s is the CTA's slot i = s + k * stages (its
@@ -545,8 +552,9 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const int u = fwd_slot_unit(p, i);
         if (u < 0) break;
         const int s = i % p.stages, k = i / p.stages;
-        if (k >= 1 && !mbar_wait(&empty_bar[s], (k - 1) & 1)) return;
-        if (!mbar_wait(&full_bar[s], k & 1)) return;
+        // the consumers meet at no named barrier, so a group that gave up may leave
+        if (k >= 1 && !mbar_wait(&empty_bar[s], (k - 1) & 1, &s_abort)) return;
+        if (!mbar_wait(&full_bar[s], k & 1, &s_abort)) return;
         const Unit g = s_unit[s];
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         if constexpr (GT) {
@@ -1041,6 +1049,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     __shared__ int s_off[kMaxEntries];
     __shared__ int s_start[kMaxHeads + 1];   // the heads' table starts (per-unit reads from shared memory)
     __shared__ int s_gt_count;               // fused global token: dense-sum items done in this unit
+    __shared__ int s_abort;                  // a bounded wait of this CTA gave up (mbar_wait)
 
     const int N = tab.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1066,6 +1075,7 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             mbar_init(&aux_bar[s], 1);
         }
         s_gt_count = 0;
+        s_abort = 0;
     }
     __syncthreads();
     grid_dep_wait();
@@ -1079,7 +1089,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         int i = 0;
         for (int it = blockIdx.x; it < p.n_units; it += gridDim.x, ++i) {
             const int s = i % p.stages;
-            if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1)) return;
+            // the lanes agree, so the warp leaves the loop together
+            if (i >= p.stages && !__all_sync(kFullMask, mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1, &s_abort)))
+                break;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const bool fill_by_consumers = i == 0;
             const size_t row0 = (size_t)bwd_item_unit(p, it) * N;
@@ -1111,7 +1123,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 if (lane == 0) mbar_arrive(&aux_bar[s]);
                 continue;
             }
-            if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
+            if (!__all_sync(kFullMask, mbar_wait(&full_bar[s], (i / p.stages) & 1, &s_abort))) {
+                ++i;   // this unit's copies were issued
+                break;
+            }
             float *sD = reinterpret_cast<float *>(st + 4 * tens), *sL = sD + N;
             // kDRows rows per lane and step, every dot product formed before
             // any store, so the rows' global loads are in flight together
@@ -1135,6 +1150,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&aux_bar[s]);
         }
+        // i units issued: leave only once the last copies into every stage
+        // have landed
+        if (lane == 0)
+            for (int s = 0; s < p.stages && s < i; ++s) mbar_drain(&full_bar[s], ((i - 1 - s) / p.stages) & 1);
         return;
     }
     const int cw = warp - 1;
@@ -1146,8 +1165,12 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
     int i = 0;
     for (int it = blockIdx.x; it < p.n_units; it += gridDim.x, ++i) {
         const int s = i % p.stages;
-        if (!mbar_wait(&full_bar[s], (i / p.stages) & 1)) return;
-        if (!mbar_wait(&aux_bar[s], (i / p.stages) & 1)) return;
+        // A failed wait does not end the warp: the consumers meet at named
+        // barriers, so every warp carries on (every later wait of the CTA
+        // then returns at once) and all of them leave together.  What they
+        // compute after a failure is never trusted: the error word is set.
+        mbar_wait(&full_bar[s], (i / p.stages) & 1, &s_abort);
+        mbar_wait(&aux_bar[s], (i / p.stages) & 1, &s_abort);
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         const uint8_t *sQ = st, *sK = st + tens;
         const float *sD = reinterpret_cast<const float *>(st + 4 * tens), *sL = sD + N;

@@ -3,8 +3,9 @@
 //
 // Every wait on an mbarrier is bounded by wall-clock time (%globaltimer):
 // after kWaitLimitNs the waiting thread records kErrWaitTimeout in the
-// device error word and the kernel returns, so a bad byte count can never hang
-// the GPU.
+// device error word and raises the CTA's abort flag, after which no wait of
+// the CTA blocks any more, so a bad byte count can never hang the GPU; a
+// producer still waits (bounded) for the copies it issued before it leaves.
 #pragma once
 
 #include <cstdint>
@@ -19,6 +20,7 @@ namespace fibatt {
 // Only resident.cu includes this header, so the word has one definition.
 static __device__ unsigned int g_device_error = 0;
 constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned kErrDrainTimeout = 2u;   // a producer left before its last copies landed
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -76,6 +78,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // recorded).  Each try_wait carries a suspend-time hint, so a waiting warp is
 // parked by the hardware until the phase completes (or about 0.5 ms pass)
 // instead of spinning and taking issue slots from the warps that compute.
+//
+// `abort` is a flag in the CTA's shared memory.  A wait that runs out of time
+// sets it, and every wait of the CTA that starts (or is still spinning) once
+// it is set gives up at once.  So when one wait fails, the whole CTA stops
+// waiting: a caller that carries on after a false return (computing garbage
+// that is never trusted, since the error word is set) still reaches every
+// named barrier its peers reach, and no warp is left behind at one.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t b, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -86,15 +95,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t b, uint32_t parity) {
     return done != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     const uint32_t b = smem_u32(bar);
+    if (*abort) return false;
     if (mbar_try_wait(b, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         if (mbar_try_wait(b, parity)) return true;
+        if (*abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             atomicOr(&g_device_error, kErrWaitTimeout);
+            *abort = 1;
             return false;
+        }
+    }
+}
+
+// Wait, bounded but regardless of `abort`, for phase `parity` of a stage's
+// "full" barrier: the bulk copies a producer issued into the stage have
+// landed.  A producer calls it for the last use of every stage before it
+// leaves, so the CTA never exits with copies still writing into its shared
+// memory (its consumers may have given up on them).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const uint32_t b = smem_u32(bar);
+    if (mbar_try_wait(b, parity)) return;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(b, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_device_error, kErrDrainTimeout);
+            return;
         }
     }
 }

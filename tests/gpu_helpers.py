@@ -84,6 +84,22 @@ def pick_rows(N, count, seed):
     return sorted({r for r in edge + rnd if 0 <= r < N})
 
 
+def band_edge_rows(N, head, w, count, seed):
+    """Rows where a head's band changes: the sequence ends, the window edges
+    (w - 1, w, N - 1 - w, N - w) and, for every distance f of the head's
+    table, the rows next to f and N - 1 - f, where the key j + f (or j - f)
+    enters or leaves [0, N); topped up with a seeded random sample."""
+    dist = sorted({abs(int(d)) for d in oracle.signed_table(N, head) if d != 0})
+    cand = {0, 1, 2, N // 2, N - 3, N - 2, N - 1, w - 1, w, N - 1 - w, N - w}
+    for f in dist:
+        cand |= {f - 1, f, f + 1, N - 2 - f, N - 1 - f, N - f}
+    rows = {r for r in cand if 0 <= r < N}
+    rng = np.random.default_rng(seed)
+    while len(rows) < min(N, count):
+        rows.add(int(rng.integers(0, N)))
+    return sorted(rows)
+
+
 def run_fwd(wl, sup, q, k, v):
     qd, kd, vd = to_dev(q, k, v)
     O, L = api.fwd(sup, qd, kd, vd, wl.scale)
@@ -92,4 +108,4 @@ def run_fwd(wl, sup, q, k, v):
 
 
 __all__ = ["TOL", "oracle_heads", "support_for", "to_dev", "assert_close", "assert_close_global", "pick_rows",
-           "run_fwd", "make_inputs"]
+           "band_edge_rows", "run_fwd", "make_inputs"]

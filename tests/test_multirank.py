@@ -48,6 +48,42 @@ def test_two_gloo_ranks_take_the_slowest_time():
         assert value == pytest.approx(2 * 1000 * 4 / 0.015)
 
 
+def _stub_arm(args):
+    """The CUDA arm stood in for by its host logic on gloo: each rank reports
+    the slowest rank's time and the whole-job value."""
+    import torch
+    import bench
+    world, rank, local = bench.dist_env()
+    bench.init_dist(world, "gloo")
+    bench.barrier(world)
+    slowest = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+    value = bench.whole_job_value(1000, 4, world, slowest)
+    with open(os.path.join(args.out_dir, f"rank{rank}.txt"), "w") as f:
+        f.write(f"{rank} {local} {world} {slowest} {value}")
+    torch.distributed.destroy_process_group()
+
+
+def test_launcher_starts_one_rank_per_gpu(tmp_path, monkeypatch):
+    # bench.py --gpus 2 without torchrun: bench starts the two ranks itself
+    import bench
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    args = bench.parse_args(["--gpus", "2"])
+    args.out_dir = str(tmp_path)
+    bench.launch_ranks(2, _stub_arm, args)
+    got = sorted((tmp_path / f"rank{r}.txt").read_text().split() for r in range(2))
+    for r, (rank, local, world, slowest, value) in enumerate(got):
+        assert int(rank) == r and int(local) == r and int(world) == 2
+        assert float(slowest) == 15.0
+        assert float(value) == pytest.approx(2 * 1000 * 4 / 0.015)
+
+
+def test_gpus_must_match_torchrun_world(monkeypatch):
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    with pytest.raises(SystemExit, match="WORLD_SIZE=1"):
+        bench.main(["--gpus", "2"])
+
+
 def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     import bench
     monkeypatch.setenv("RANK", "1")

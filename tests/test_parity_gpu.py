@@ -10,8 +10,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (assert_close, assert_close_global, make_inputs, oracle_heads, pick_rows,
-                         support_for, to_dev)
+from gpu_helpers import (assert_close, assert_close_global, band_edge_rows, make_inputs, oracle_heads,
+                         pick_rows, support_for, to_dev)
 from sparse_head_self_gb300 import api
 from sparse_head_self_gb300.inputs import WORKLOADS, Workload
 
@@ -459,13 +459,39 @@ def _sampled(wl, nbh, nrows, seed, backward):
             assert_close(f"{wl.name} dV[{b},{h}]", dV[b, h, rows].float().cpu(), rV, wl.dtype)
 
 
-def test_video_full_size_fwd_sampled():
-    _sampled(WORKLOADS["video"], nbh=12, nrows=48, seed=101, backward=True)
+def _every_head_band_edges(wl, nrows, seed):
+    """Every (b, h) head of the workload at full size, in the bench's launch
+    configuration: forward and backward outputs on each head's band-edge rows
+    (band_edge_rows) plus a seeded sample, element by element."""
+    q, k, v, do = make_inputs(wl, 0)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    torch.cuda.synchronize()
+    O, L, dQ, dK, dV = (x.float().cpu() for x in (O, L, dQ, dK, dV))
+    heads = oracle_heads(wl)
+    w = oracle.windows(wl.H, wl.w_min, wl.w_max)
+    for h in range(wl.H):
+        rows = band_edge_rows(wl.N, heads[h], w[h], nrows, seed + h)
+        for b in range(wl.B):
+            Or, Lr = oracle.fwd_head(q[b, h], k[b, h], v[b, h], heads[h], wl.scale, rows=rows)
+            rQ, rK, rV = oracle.bwd_head(q[b, h], k[b, h], v[b, h], do[b, h], heads[h], wl.scale,
+                                         qrows=rows, krows=rows)
+            assert_close(f"{wl.name} O[{b},{h}]", O[b, h, rows], Or, wl.dtype)
+            assert_close(f"{wl.name} LSE[{b},{h}]", L[b, h, rows], Lr, wl.dtype, lse=True)
+            assert_close(f"{wl.name} dQ[{b},{h}]", dQ[b, h, rows], rQ, wl.dtype)
+            assert_close(f"{wl.name} dK[{b},{h}]", dK[b, h, rows], rK, wl.dtype)
+            assert_close(f"{wl.name} dV[{b},{h}]", dV[b, h, rows], rV, wl.dtype)
+
+
+def test_video_full_size_every_head_band_edges():
+    _every_head_band_edges(WORKLOADS["video"], nrows=64, seed=101)
 
 
 def test_train_full_size_fwd_bwd_sampled():
     _sampled(WORKLOADS["train"], nbh=24, nrows=40, seed=202, backward=True)
 
 
-def test_long_full_size_fwd_bwd_sampled():
-    _sampled(WORKLOADS["long"], nbh=6, nrows=12, seed=303, backward=True)
+def test_long_full_size_every_head_band_edges():
+    _every_head_band_edges(WORKLOADS["long"], nrows=48, seed=303)
