@@ -141,6 +141,12 @@ cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl);
 cudaError_t launch_fwd_flat(const FwdArgs &a);
 cudaError_t launch_bwd_flat(const BwdArgs &a);       // a.Dws: pair-weight scratch
 size_t flat_bwd_scratch_bytes(const TableArg &tab, int B);
+// Streaming kernels for wide windows (stream.cu): rows 32-byte aligned, no
+// global first token.  The backward's workspace: D_j per row, then dS per
+// (b, h, table entry, query row).
+cudaError_t launch_fwd_stream(const FwdArgs &a);
+cudaError_t launch_bwd_stream(const BwdArgs &a);
+size_t stream_bwd_scratch_bytes(const TableArg &tab, int B);
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
 

@@ -32,6 +32,7 @@
 // global memory, for heads whose key windows do not fit in shared memory.
 #include <algorithm>
 #include <cstdlib>
+#include <initializer_list>
 #include <type_traits>
 
 #include "fibatt_internal.h"
@@ -1857,7 +1858,18 @@ static cudaError_t bwd_flat(const BwdArgs &a, int bh0, int count) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The streaming kernels (stream.cu) need 32-byte aligned rows (256-bit
+// accesses); FIBATT_STREAM=0 selects the kernels below for every call.
+static bool use_stream(const TableArg &tab, std::initializer_list<const void *> ptrs) {
+    const char *e = getenv("FIBATT_STREAM");
+    if (tab.global0 || (e && atoi(e) == 0)) return false;
+    for (const void *q : ptrs)
+        if (reinterpret_cast<uintptr_t>(q) % 32 != 0) return false;
+    return true;
+}
+
 cudaError_t launch_bwd_flat(const BwdArgs &a) {
+    if (use_stream(*a.tab, {a.Q, a.K, a.V, a.O, a.dO, a.dQ, a.dK, a.dV})) return launch_bwd_stream(a);
     int G = 4;
     if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
     const int units = a.B * a.tab->H;
@@ -1869,7 +1881,8 @@ cudaError_t launch_bwd_flat(const BwdArgs &a) {
 }
 
 size_t flat_bwd_scratch_bytes(const TableArg &tab, int B) {
-    return (size_t)B * tab.H * 2 * std::max(1, (int)tab.max_count) * tab.N * sizeof(float);
+    return std::max(stream_bwd_scratch_bytes(tab, B),
+                    (size_t)B * tab.H * 2 * std::max(1, (int)tab.max_count) * tab.N * sizeof(float));
 }
 
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl) {
@@ -1896,6 +1909,7 @@ static cudaError_t fwd_flat(const FwdArgs &a) {
 }
 
 cudaError_t launch_fwd_flat(const FwdArgs &a) {
+    if (use_stream(*a.tab, {a.Q, a.K, a.V, a.O})) return launch_fwd_stream(a);
     int G = 4;   // four lanes per row: more warps in flight to cover global-load latency (measured faster)
     if (const char *e = getenv("FIBATT_FLAT_LANES")) G = atoi(e) == 2 ? 2 : 4;
     if (a.tab->global0)

@@ -1,0 +1,504 @@
+// Streaming Fibottention kernels: the banded forward and backward for heads
+// whose key windows do not fit in shared memory (long sequences with wide
+// windows, e.g. 8 video frames of 196 patches, or 128 x 128 patches).
+//
+// Every row comes straight from global memory through L1/L2.  A row is
+// 64 elements; G lanes share it, lane `sub` owning one contiguous run of
+// 64/G dims, read with 256-bit loads (ld.global.nc.v8.b32) so that the G
+// lanes of a row cover the whole row in full 32-byte sectors.  (Slices whose
+// 16-byte pieces alternate between lanes touch every sector twice per row.)
+// Blocks are numbered head-major: all row blocks of one (b, h) run next to
+// each other, so the K/V rows the resident blocks reach -- one head's, a few
+// MB -- stay in L2 instead of the rows of every head at once.
+//
+// Forward (Fibottention Sec. 3; README Algorithm 3 restricted to the
+// support): query row j, offsets off[t] of its head, key k = j + off[t]:
+//   s = scale <q_j, k_k>, online softmax in log2 units, O_j = sum P v_k / l,
+//   LSE_j = ln l + max.
+// Backward, three launches, no atomics:
+//   LSE_j log2(e) and D_j = <dO_j, O_j> for every row;
+//   key-centric (key k stationary in registers; queries j = k + off[t], the
+//   table being symmetric): P = exp(s - LSE_j), dS = P (<dO_j, v_k> - D_j),
+//   dV_k = sum P dO_j, dK_k = scale sum dS q_j, and dS of each pair into a
+//   scratch indexed by the query's own table entry;
+//   query-centric: dQ_j = scale sum dS k_k over the same pairs.
+// So the backward reads q, dO (key pass) and k (query pass) per pair: three
+// rows instead of four, and one fp32 of scratch each way.
+#include <algorithm>
+#include <cstdlib>
+#include <type_traits>
+
+#include "fibatt_internal.h"
+#include "row_math.cuh"
+
+namespace fibatt {
+namespace {
+
+// Warps per block (consecutive row groups of one head).  Larger blocks
+// raise the L1 hits between neighbouring offsets (the 128 x 128 image shape's
+// forward: L2-to-SM bytes 2.80 -> 2.44 GB with 8 warps) but hold fewer warps
+// per SM at these register counts, which costs more: 4 measured fastest.
+constexpr int kStreamWarps = 4;
+
+// 256-bit read-only load and store of eight 32-bit words (32-byte aligned).
+__device__ __forceinline__ void ld8(const uint8_t *p, uint32_t *w) {
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                   "=r"(w[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st8(uint8_t *p, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// One lane's contiguous slice of a 64-dim row (64/G elements, as 32-bit
+// words: packed bf16 pairs or fp32 values), and the matching fp32
+// accumulator layout (float2 per element pair, in dim order).
+template <typename T, int G>
+struct Run {
+    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    static constexpr int kRowBytes = 64 * (int)sizeof(T);
+    static constexpr int kBytes = kRowBytes / G;    // bytes of the slice: 32 or 64
+    static constexpr int kWords = kBytes / 4;
+    static constexpr int kPairs = 32 / G;           // float2 accumulators
+    static_assert(kBytes % 32 == 0, "a slice is whole 256-bit loads");
+    uint32_t w[kWords];
+
+    __device__ __forceinline__ void load(const uint8_t *p) {
+#pragma unroll
+        for (int i = 0; i < kWords / 8; ++i) ld8(p + 32 * i, w + 8 * i);
+    }
+    // partial dot product over this lane's dims (four sums for ILP)
+    __device__ __forceinline__ float dot(const Run &o) const {
+        float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
+        if constexpr (kBf16) {
+#pragma unroll
+            for (int i = 0; i < kWords; i += 4) {
+                a = dot2_bf16(w[i], o.w[i], a);
+                b = dot2_bf16(w[i + 1], o.w[i + 1], b);
+                c = dot2_bf16(w[i + 2], o.w[i + 2], c);
+                d = dot2_bf16(w[i + 3], o.w[i + 3], d);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kWords; i += 4) {
+                a = fmaf(__uint_as_float(w[i]), __uint_as_float(o.w[i]), a);
+                b = fmaf(__uint_as_float(w[i + 1]), __uint_as_float(o.w[i + 1]), b);
+                c = fmaf(__uint_as_float(w[i + 2]), __uint_as_float(o.w[i + 2]), c);
+                d = fmaf(__uint_as_float(w[i + 3]), __uint_as_float(o.w[i + 3]), d);
+            }
+        }
+        return (a + b) + (c + d);
+    }
+    // acc += p * this (fp32 weight)
+    __device__ __forceinline__ void axpy(float p, float2 (&acc)[kPairs]) const {
+        const float2 pp = make_float2(p, p);
+        if constexpr (kBf16) {
+#pragma unroll
+            for (int i = 0; i < kWords; ++i) acc[i] = fma2(pp, make_float2(bf16_lo(w[i]), bf16_hi(w[i])), acc[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPairs; ++i)
+                acc[i] = fma2(pp, make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1])), acc[i]);
+        }
+    }
+    // acc += p2 * this for a weight already rounded to bf16 (both halves of
+    // p2); bf16 rows only: one mixed-precision FMA per element
+    __device__ __forceinline__ void axpy_p2(uint32_t p2, float2 (&acc)[kPairs]) const {
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) acc[i] = fma2_bf16(p2, w[i], acc[i]);
+    }
+    // acc * s to the I/O dtype (RNE for bf16), stored at p
+    __device__ __forceinline__ static void store(uint8_t *p, const float2 (&acc)[kPairs], float s) {
+        uint32_t o[kWords];
+        if constexpr (kBf16) {
+#pragma unroll
+            for (int i = 0; i < kWords; ++i) o[i] = pack_bf16x2(acc[i].x * s, acc[i].y * s);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPairs; ++i) {
+                o[2 * i] = __float_as_uint(acc[i].x * s);
+                o[2 * i + 1] = __float_as_uint(acc[i].y * s);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kWords / 8; ++i) st8(p + 32 * i, o + 8 * i);
+    }
+};
+
+template <int G>
+__device__ __forceinline__ float lanes_sum(float x) {
+#pragma unroll
+    for (int m = 1; m < G; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+// Entries [tb, te) of the head's ascending offsets off[0, cnt) that reach a
+// row in [0, N) from at least one of the rows [first, last]: the others are
+// dropped for the whole warp.  Warp-collective.
+__device__ __forceinline__ void trim(const int *off, int cnt, int N, int first, int last, int &tb, int &te) {
+    const int lane = threadIdx.x & 31;
+    int below = 0, above = 0;
+    for (int base = 0; base < cnt; base += 32) {
+        const int t = base + lane;
+        const bool e = t < cnt;
+        const int o = e ? off[t] : 0;
+        below += __popc(__ballot_sync(kFullMask, e && last + o < 0));
+        above += __popc(__ballot_sync(kFullMask, e && first + o >= N));
+    }
+    tb = below;
+    te = max(tb, cnt - above);
+}
+
+// Copy of head h's offsets into shared memory; returns the count.
+__device__ __forceinline__ int load_offsets(const TableArg &tab, int h, int *s_off) {
+    const int t0 = tab.start[h], cnt = tab.start[h + 1] - t0;
+    for (int t = threadIdx.x; t < cnt; t += blockDim.x) s_off[t] = tab.off[t0 + t];
+    __syncthreads();
+    return cnt;
+}
+
+struct StreamParams {
+    const void *Q, *K, *V, *O, *dO;
+    const float *LSE;
+    void *Out, *dK, *dV;   // forward: O; backward: dQ (query pass) or nothing
+    float *LSEout;         // forward: LSE
+    float2 *LD;            // backward: (LSE_j log2(e), D_j) per row
+    float *scr;            // backward: dS per (b, h, table entry, query row)
+    float scale, scale_log2;
+    int nblk;              // row blocks per (b, h)
+    int max_count;         // scratch entries per (b, h)
+};
+
+// Running maximum start: finite, so a masked score (-inf) gives weight 0.
+constexpr float kMInit = -1.0e30f;
+
+// ------------------------------------------------------------------ forward
+
+template <typename T, int G, int W, bool W16>
+__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? (24 / W > 0 ? 24 / W : 1) : (16 / W > 0 ? 16 / W : 1))
+fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
+    using S = Run<T, G>;
+    constexpr int R = 32 / G;
+    constexpr int RB = S::kRowBytes;
+    extern __shared__ int s_off[];
+    const int N = tab.N;
+    const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
+    const int cnt = load_offsets(tab, bh % tab.H, s_off);
+    grid_dep_wait();
+    grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % G;
+    const int first = (yb * W + warp) * R;
+    if (first >= N) return;   // the whole warp
+    const int last = min(N, first + R) - 1;
+    const bool valid = first + lane / G < N;
+    const int j = valid ? first + lane / G : last;
+    int tb, te;
+    trim(s_off, cnt, N, first, last, tb, te);
+
+    const size_t row0 = (size_t)bh * N;
+    const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB + sub * S::kBytes;
+    const uint8_t *gV = static_cast<const uint8_t *>(p.V) + row0 * RB + sub * S::kBytes;
+    S q;
+    q.load(static_cast<const uint8_t *>(p.Q) + (row0 + j) * RB + sub * S::kBytes);
+    float2 acc[S::kPairs];
+#pragma unroll
+    for (int i = 0; i < S::kPairs; ++i) acc[i] = make_float2(0.f, 0.f);
+    float m = kMInit, l = 0.f, lt = 0.f;   // lt: the weights as they entered acc (bf16-rounded with W16)
+    const float sl2 = p.scale_log2;
+    auto raise = [&](float s) {
+        if (s > m + 8.f) {   // rare: p = 2^(s - m) <= 2^8 between raises
+            const float a = fast_exp2(m - s);
+            l *= a;
+            lt *= a;
+#pragma unroll
+            for (int i = 0; i < S::kPairs; ++i) acc[i] = mul2(acc[i], make_float2(a, a));
+            m = s;
+        }
+    };
+    auto add = [&](const S &v, float pr) {
+        l += pr;
+        if constexpr (W16 && S::kBf16) {
+            const uint32_t p2 = bf16x2_splat(pr);
+            lt += __uint_as_float(p2 << 16);
+            v.axpy_p2(p2, acc);
+        } else {
+            v.axpy(pr, acc);
+        }
+    };
+    int t = tb;
+    for (; t + 1 < te; t += 2) {   // two offsets per step: four row loads in flight
+        const int k0 = j + s_off[t], k1 = j + s_off[t + 1];
+        const bool in0 = valid && k0 >= 0 && k0 < N, in1 = valid && k1 >= 0 && k1 < N;
+        const size_t c0 = (size_t)min(max(k0, 0), N - 1) * RB, c1 = (size_t)min(max(k1, 0), N - 1) * RB;
+        S ka, kb, va, vb;
+        ka.load(gK + c0);
+        kb.load(gK + c1);
+        va.load(gV + c0);
+        vb.load(gV + c1);
+        float s0 = lanes_sum<G>(q.dot(ka)) * sl2, s1 = lanes_sum<G>(q.dot(kb)) * sl2;
+        s0 = in0 ? s0 : -INFINITY;
+        s1 = in1 ? s1 : -INFINITY;
+        raise(fmaxf(s0, s1));
+        add(va, fast_exp2(s0 - m));
+        add(vb, fast_exp2(s1 - m));
+    }
+    if (t < te) {
+        const int k0 = j + s_off[t];
+        const bool in0 = valid && k0 >= 0 && k0 < N;
+        const size_t c0 = (size_t)min(max(k0, 0), N - 1) * RB;
+        S ka, va;
+        ka.load(gK + c0);
+        va.load(gV + c0);
+        float s0 = lanes_sum<G>(q.dot(ka)) * sl2;
+        s0 = in0 ? s0 : -INFINITY;
+        raise(s0);
+        add(va, fast_exp2(s0 - m));
+    }
+    if (!valid) return;
+    const float ln = (W16 && S::kBf16) ? lt : l;
+    S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + sub * S::kBytes, acc, ln > 0.f ? __frcp_rn(ln) : 0.f);
+    if (sub == 0) p.LSEout[row0 + j] = l > 0.f ? (m + fast_log2(l)) * kLn2 : -INFINITY;
+}
+
+// ----------------------------------------------------------------- backward
+
+// Per row: LSE_j log2(e) and D_j = <dO_j, O_j>, rows [0, rows).
+template <typename T, int G, int W>
+__global__ void __launch_bounds__(W * 32) rowdot_stream_kernel(const StreamParams p, long rows) {
+    using S = Run<T, G>;
+    constexpr int RB = S::kRowBytes;
+    grid_dep_wait();
+    grid_dep_launch();
+    const int lane = threadIdx.x & 31, sub = lane % G;
+    const long r = ((long)blockIdx.x * W + (threadIdx.x >> 5)) * (32 / G) + lane / G;
+    const long rc = r < rows ? r : rows - 1;
+    S o, g;
+    o.load(static_cast<const uint8_t *>(p.O) + rc * RB + sub * S::kBytes);
+    g.load(static_cast<const uint8_t *>(p.dO) + rc * RB + sub * S::kBytes);
+    const float l = p.LSE[rc];
+    const float d = lanes_sum<G>(o.dot(g));
+    if (r < rows && sub == 0) p.LD[r] = make_float2(l * kLog2e, d);
+}
+
+// Key-centric pass: key row k stationary; the queries attending it are
+// j = k + off[t] (symmetric table), whose pair is query j's entry cnt-1-t.
+template <typename T, int G, int W>
+__global__ void __launch_bounds__(W * 32)
+bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
+    using S = Run<T, G>;
+    constexpr int R = 32 / G;
+    constexpr int RB = S::kRowBytes;
+    extern __shared__ int s_off[];
+    const int N = tab.N;
+    const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
+    const int cnt = load_offsets(tab, bh % tab.H, s_off);
+    grid_dep_wait();
+    grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % G;
+    const int first = (yb * W + warp) * R;
+    if (first >= N) return;
+    const int last = min(N, first + R) - 1;
+    const bool valid = first + lane / G < N;
+    const int k = valid ? first + lane / G : last;
+    int tb, te;
+    trim(s_off, cnt, N, first, last, tb, te);
+
+    const size_t row0 = (size_t)bh * N;
+    const size_t lo = sub * S::kBytes;
+    const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB + lo;
+    const uint8_t *gG = static_cast<const uint8_t *>(p.dO) + row0 * RB + lo;
+    const float2 *ld = p.LD + row0;
+    float *scr = p.scr + (size_t)bh * p.max_count * N + (size_t)(cnt - 1) * N;   // entry cnt-1-t at -t N
+    float2 dk[S::kPairs], dv[S::kPairs];
+#pragma unroll
+    for (int i = 0; i < S::kPairs; ++i) dk[i] = dv[i] = make_float2(0.f, 0.f);
+    const float sl2 = p.scale_log2;
+    S kk, vv;
+    kk.load(static_cast<const uint8_t *>(p.K) + (row0 + k) * RB + lo);
+    vv.load(static_cast<const uint8_t *>(p.V) + (row0 + k) * RB + lo);
+    for (int t = tb; t < te; ++t) {
+        const int j = k + s_off[t];
+        const bool in = valid && (unsigned)j < (unsigned)N;
+        const int jc = in ? j : k;   // any row in range: its pair is masked
+        S qq, gg;
+        qq.load(gQ + (size_t)jc * RB);
+        gg.load(gG + (size_t)jc * RB);
+        const float2 lj = ld[jc];
+        const float s = lanes_sum<G>(qq.dot(kk));
+        const float dp = lanes_sum<G>(gg.dot(vv));
+        const float P = in ? fast_exp2(fmaf(s, sl2, -lj.x)) : 0.f;
+        const float dS = P * (dp - lj.y);
+        // fp32 weights: bf16-rounded P and dS (one mixed-precision FMA per
+        // element instead of an unpack and half a packed FMA) put the dK and
+        // dQ errors within a few thousandths of the bf16 bound
+        gg.axpy(P, dv);
+        qq.axpy(dS, dk);
+        if (in && sub == 0) scr[(ptrdiff_t)j - (ptrdiff_t)t * N] = dS;
+    }
+    if (!valid) return;
+    S::store(static_cast<uint8_t *>(p.dK) + (row0 + k) * RB + lo, dk, p.scale);
+    S::store(static_cast<uint8_t *>(p.dV) + (row0 + k) * RB + lo, dv, 1.f);
+}
+
+// Query-centric pass: dQ_j = scale sum over in-range entries t of
+// dS(j, t) k_{j + off[t]}, dS from the key pass's scratch.
+template <typename T, int G, int W>
+__global__ void __launch_bounds__(W * 32)
+bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
+    using S = Run<T, G>;
+    constexpr int R = 32 / G;
+    constexpr int RB = S::kRowBytes;
+    extern __shared__ int s_off[];
+    const int N = tab.N;
+    const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
+    const int cnt = load_offsets(tab, bh % tab.H, s_off);
+    grid_dep_wait();
+    grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % G;
+    const int first = (yb * W + warp) * R;
+    if (first >= N) return;
+    const int last = min(N, first + R) - 1;
+    const bool valid = first + lane / G < N;
+    const int j = valid ? first + lane / G : last;
+    int tb, te;
+    trim(s_off, cnt, N, first, last, tb, te);
+
+    const size_t row0 = (size_t)bh * N;
+    const size_t lo = sub * S::kBytes;
+    const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB + lo;
+    const float *scr = p.scr + (size_t)bh * p.max_count * N + j;
+    float2 dq[S::kPairs];
+#pragma unroll
+    for (int i = 0; i < S::kPairs; ++i) dq[i] = make_float2(0.f, 0.f);
+    // four offsets per step: their key-row and weight loads all in flight
+    // before the first update
+    constexpr int U = 4;
+    int t = tb;
+    for (; t + U <= te; t += U) {
+        S kr[U];
+        float wt[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int kk = j + s_off[t + u];
+            const bool in = valid && (unsigned)kk < (unsigned)N;
+            kr[u].load(gK + (size_t)(in ? kk : j) * RB);
+            // out-of-range entries were never written: select, never multiply
+            wt[u] = in ? scr[(size_t)(t + u) * N] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) kr[u].axpy(wt[u], dq);
+    }
+    for (; t < te; ++t) {
+        const int kk = j + s_off[t];
+        const bool in = valid && (unsigned)kk < (unsigned)N;
+        S kr;
+        kr.load(gK + (size_t)(in ? kk : j) * RB);
+        const float w0 = in ? scr[(size_t)t * N] : 0.f;
+        kr.axpy(w0, dq);
+    }
+    if (!valid) return;
+    S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + lo, dq, p.scale);
+}
+
+int stream_lanes() {
+    const char *e = getenv("FIBATT_FLAT_LANES");
+    return (e && atoi(e) == 2) ? 2 : 4;
+}
+
+// bf16 weights in the forward's P.V update (FIBATT_FLAT_W16=0: fp32
+// weights); measured faster on the 128 x 128 image shape
+bool stream_w16() {
+    const char *e = getenv("FIBATT_FLAT_W16");
+    return !(e && atoi(e) == 0);
+}
+
+template <typename T, int G, bool W16, int W = kStreamWarps>
+cudaError_t fwd_stream(const FwdArgs &a) {
+    constexpr int R = 32 / G;
+    const TableArg &tab = *a.tab;
+    StreamParams p{};
+    p.Q = a.Q;
+    p.K = a.K;
+    p.V = a.V;
+    p.Out = a.O;
+    p.LSEout = a.LSE;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.nblk = (tab.N + R * W - 1) / (R * W);
+    const size_t smem = sizeof(int) * std::max(1, (int)tab.max_count);
+    const cudaError_t e = launch_kernel(fwd_stream_kernel<T, G, W, W16>, dim3((unsigned)((long)a.B * tab.H * p.nblk)),
+                                        dim3(W * 32), smem, a.stream, pdl_enabled(), tab, p);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <typename T, int G, int W = kStreamWarps>
+cudaError_t bwd_stream(const BwdArgs &a) {
+    constexpr int R = 32 / G;
+    const TableArg &tab = *a.tab;
+    const long rows = (long)a.B * tab.H * tab.N;
+    StreamParams p{};
+    p.Q = a.Q;
+    p.K = a.K;
+    p.V = a.V;
+    p.O = a.O;
+    p.dO = a.dO;
+    p.LSE = a.LSE;
+    p.dK = a.dK;
+    p.dV = a.dV;
+    p.LD = reinterpret_cast<float2 *>(a.Dws);
+    p.scr = a.Dws + (2 * rows + 63) / 64 * 64;   // 256-byte aligned, after LD
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.nblk = (tab.N + R * W - 1) / (R * W);
+    p.max_count = std::max(1, (int)tab.max_count);
+    const bool pdl = pdl_enabled();
+    const size_t smem = sizeof(int) * p.max_count;
+    const dim3 block(W * 32);
+    const unsigned row_blocks = (unsigned)((rows + R * W - 1) / (R * W));
+    const unsigned blocks = (unsigned)((long)a.B * tab.H * p.nblk);
+    cudaError_t e = launch_kernel(rowdot_stream_kernel<T, G, W>, dim3(row_blocks), block, 0, a.stream, pdl, p, rows);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = launch_kernel(bwd_key_stream_kernel<T, G, W>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    p.Out = a.dQ;
+    if (e == cudaSuccess)
+        e = launch_kernel(bwd_query_stream_kernel<T, G, W>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
+    count_launches(3);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+// Warps per block (FIBATT_STREAM_WARPS: 4 or 8).
+int stream_warps() {
+    const char *e = getenv("FIBATT_STREAM_WARPS");
+    return e && atoi(e) == 8 ? 8 : kStreamWarps;
+}
+
+cudaError_t launch_fwd_stream(const FwdArgs &a) {
+    const bool w16 = stream_w16();
+    if (a.dtype == FIBATT_F32) return fwd_stream<float, 4, false>(a);
+    if (stream_lanes() == 2)
+        return w16 ? fwd_stream<__nv_bfloat16, 2, true>(a) : fwd_stream<__nv_bfloat16, 2, false>(a);
+    if (!w16) return fwd_stream<__nv_bfloat16, 4, false>(a);
+    return stream_warps() == 8 ? fwd_stream<__nv_bfloat16, 4, true, 8>(a) : fwd_stream<__nv_bfloat16, 4, true, 4>(a);
+}
+
+cudaError_t launch_bwd_stream(const BwdArgs &a) {
+    if (a.dtype == FIBATT_F32) return bwd_stream<float, 4>(a);
+    if (stream_lanes() == 2) return bwd_stream<__nv_bfloat16, 2>(a);
+    return stream_warps() == 8 ? bwd_stream<__nv_bfloat16, 4, 8>(a) : bwd_stream<__nv_bfloat16, 4, 4>(a);
+}
+
+size_t stream_bwd_scratch_bytes(const TableArg &tab, int B) {
+    const size_t rows = (size_t)B * tab.H * tab.N;
+    return ((2 * rows + 63) / 64 * 64 + (size_t)B * tab.H * std::max(1, (int)tab.max_count) * tab.N) * sizeof(float);
+}
+
+}  // namespace fibatt

@@ -27,8 +27,12 @@ def kernel_path(request, monkeypatch):
     resident arithmetic on rows read from global memory; backward generic)
     or auto (the library's choice)."""
     path = getattr(request, "param", "auto")
+    monkeypatch.delenv("FIBATT_STREAM", raising=False)
     if path == "auto":
         monkeypatch.delenv("FIBATT_PATH", raising=False)
+    elif path == "flat_legacy":   # the flat kernels that predate the streaming ones
+        monkeypatch.setenv("FIBATT_PATH", "flat")
+        monkeypatch.setenv("FIBATT_STREAM", "0")
     else:
         monkeypatch.setenv("FIBATT_PATH", path)
     return path
@@ -57,12 +61,12 @@ def _bwd_full(wl, seed=0):
 
 # ------------------------------------------------------------ small, full
 
-@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat", "flat_legacy"], indirect=True)
 def test_tiny_fwd_fp32_full(kernel_path):
     _fwd_full(WORKLOADS["tiny"])
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "resident", "flat", "flat_legacy"], indirect=True)
 def test_tiny_bwd_fp32_full(kernel_path):
     _bwd_full(WORKLOADS["tiny"])
 
@@ -81,7 +85,7 @@ def test_video_shape_one_batch_fwd_full():
     _fwd_full(wl, seed=7)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "flat"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "flat_legacy"], indirect=True)
 def test_video_shape_two_heads_bwd_full(kernel_path):
     # every row of two heads (the narrowest and the widest window) of one
     # batch element: every gradient compared with the oracle's
@@ -99,7 +103,7 @@ def test_video_shape_two_heads_bwd_full(kernel_path):
         assert_close(f"video h{h} dV", dV[0, h].float().cpu(), rV, wl.dtype)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "flat", "auto"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "flat_legacy", "auto"], indirect=True)
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 63, 64, 65, 127, 129, 300])
 @pytest.mark.parametrize("diag", [False, True])
 def test_edge_sizes(N, diag, kernel_path):
@@ -109,6 +113,43 @@ def test_edge_sizes(N, diag, kernel_path):
     wl = Workload("edge", 2, H, N, 64, "f32", 1, N, diag, True)
     _fwd_full(wl, seed=N)
     _bwd_full(wl, seed=N)
+
+
+def _offset_view(t, elems):
+    """A copy of t placed `elems` elements into a larger buffer: 16-byte but
+    not 32-byte aligned when elems x element size is 16 (mod 32)."""
+    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
+    v = buf[elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_flat_rows_sixteen_byte_aligned(dtype, monkeypatch):
+    # the streaming kernels read 32-byte pieces of rows; tensors that are
+    # only 16-byte aligned (the boundary's requirement) take the older flat
+    # kernels, with the same results
+    monkeypatch.setenv("FIBATT_PATH", "flat")
+    monkeypatch.delenv("FIBATT_STREAM", raising=False)
+    wl = Workload("edge", 2, 4, 129, 64, dtype, 1, 129, True, True)
+    q, k, v, do = make_inputs(wl, 5)
+    elems = 16 // (4 if dtype == "f32" else 2)
+    qd, kd, vd, dod = (_offset_view(t.cuda(), elems) for t in (q, k, v, do))
+    assert all(t.data_ptr() % 32 == 16 for t in (qd, kd, vd, dod))
+    sup = support_for(wl)
+    O = _offset_view(torch.zeros_like(qd), elems)
+    L = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    api.fwd(sup, qd, kd, vd, wl.scale, O=O, LSE=L)
+    heads = oracle_heads(wl)
+    O_ref, L_ref = oracle.fwd(q, k, v, heads, wl.scale)
+    assert_close("O", O.float().cpu(), O_ref, wl.dtype)
+    assert_close("LSE", L.cpu(), L_ref, wl.dtype, lse=True)
+    dQ, dK, dV = (_offset_view(torch.zeros_like(qd), elems) for _ in range(3))
+    api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale, dQ=dQ, dK=dK, dV=dV)
+    rQ, rK, rV = oracle.bwd(q, k, v, do, heads, wl.scale)
+    assert_close("dQ", dQ.float().cpu(), rQ, wl.dtype)
+    assert_close("dK", dK.float().cpu(), rK, wl.dtype)
+    assert_close("dV", dV.float().cpu(), rV, wl.dtype)
 
 
 @pytest.mark.parametrize("qsplit", ["1", "2", "3", "7", "40"])
