@@ -161,13 +161,32 @@ __device__ __forceinline__ int load_offsets(const TableArg &tab, int h, int *s_o
     return cnt;
 }
 
+// L2 prefetch (a hint: nothing waits on it) of the row windows the block's
+// rows [first, first + rows) reach through each table entry, clipped to
+// [0, N): rows first + off[t] ... of the head whose row 0 is at `base`, `rb`
+// bytes per row; one entry per thread.  Every row a block reads is then on
+// its way to L2 before the block's first use of it, instead of each warp
+// meeting the compulsory misses of its own loads one step at a time.
+__device__ __forceinline__ void prefetch_windows(const uint8_t *base, int rb, const int *off, int cnt, int N,
+                                                 int first, int rows) {
+    for (int t = threadIdx.x; t < cnt; t += blockDim.x) {
+        const int lo = max(0, first + off[t]), hi = min(N, first + rows + off[t]);
+        if (hi > lo)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + (size_t)lo * rb),
+                         "r"((uint32_t)(hi - lo) * (uint32_t)rb)
+                         : "memory");
+    }
+}
+
 struct StreamParams {
     const void *Q, *K, *V, *O, *dO;
     const float *LSE;
     void *Out, *dK, *dV;   // forward: O; backward: dQ (query pass) or nothing
     float *LSEout;         // forward: LSE
     float2 *LD;            // backward: (LSE_j log2(e), D_j) per row
-    float *scr;            // backward: dS per (b, h, table entry, query row)
+    float *scr;            // backward: dS per (b, h, table entry, query row), rows of `ns` floats
+    int ns;                // scratch row stride (N rounded up to 32: 128-byte rows)
+    int prefetch;          // L2 prefetch of the block's row windows: 1 forward, 2 key pass, 4 query pass
     float scale, scale_log2;
     int nblk;              // row blocks per (b, h)
     int max_count;         // scratch entries per (b, h)
@@ -188,6 +207,14 @@ fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     const int N = tab.N;
     const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
     const int cnt = load_offsets(tab, bh % tab.H, s_off);
+    if (p.prefetch & 1) {   // Q, K and V are inputs: their rows may be prefetched into L2 while
+        // the previous kernel drains (L2 is the point of coherence, so the
+        // loads after the wait still see what that kernel wrote)
+        const size_t head = (size_t)bh * N * RB;
+        const int bfirst = yb * W * R;
+        prefetch_windows(static_cast<const uint8_t *>(p.K) + head, RB, s_off, cnt, N, bfirst, W * R);
+        prefetch_windows(static_cast<const uint8_t *>(p.V) + head, RB, s_off, cnt, N, bfirst, W * R);
+    }
     grid_dep_wait();
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % G;
@@ -296,6 +323,12 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
     const int N = tab.N;
     const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
     const int cnt = load_offsets(tab, bh % tab.H, s_off);
+    if (p.prefetch & 2) {   // the query and dO rows are inputs (see the forward)
+        const size_t head = (size_t)bh * N * RB;
+        const int bfirst = yb * W * R;
+        prefetch_windows(static_cast<const uint8_t *>(p.Q) + head, RB, s_off, cnt, N, bfirst, W * R);
+        prefetch_windows(static_cast<const uint8_t *>(p.dO) + head, RB, s_off, cnt, N, bfirst, W * R);
+    }
     grid_dep_wait();
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % G;
@@ -312,7 +345,7 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
     const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB + lo;
     const uint8_t *gG = static_cast<const uint8_t *>(p.dO) + row0 * RB + lo;
     const float2 *ld = p.LD + row0;
-    float *scr = p.scr + (size_t)bh * p.max_count * N + (size_t)(cnt - 1) * N;   // entry cnt-1-t at -t N
+    float *scr = p.scr + ((size_t)bh * p.max_count + cnt - 1) * p.ns;   // entry cnt-1-t at -t ns
     float2 dk[S::kPairs], dv[S::kPairs];
 #pragma unroll
     for (int i = 0; i < S::kPairs; ++i) dk[i] = dv[i] = make_float2(0.f, 0.f);
@@ -337,7 +370,7 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
         // dQ errors within a few thousandths of the bf16 bound
         gg.axpy(P, dv);
         qq.axpy(dS, dk);
-        if (in && sub == 0) scr[(ptrdiff_t)j - (ptrdiff_t)t * N] = dS;
+        if (in && sub == 0) scr[(ptrdiff_t)j - (ptrdiff_t)t * p.ns] = dS;
     }
     if (!valid) return;
     S::store(static_cast<uint8_t *>(p.dK) + (row0 + k) * RB + lo, dk, p.scale);
@@ -356,8 +389,21 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
     const int N = tab.N;
     const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
     const int cnt = load_offsets(tab, bh % tab.H, s_off);
+    const int bfirst = yb * W * R;
+    // the key rows are an input (see the forward); the dS rows are the key
+    // pass's output, so they wait for it
+    if (p.prefetch & 4)
+        prefetch_windows(static_cast<const uint8_t *>(p.K) + (size_t)bh * N * RB, RB, s_off, cnt, N, bfirst, W * R);
     grid_dep_wait();
     grid_dep_launch();
+    for (int t = threadIdx.x; (p.prefetch & 4) && t < cnt; t += blockDim.x) {
+        const int n = (min(N, bfirst + W * R) - bfirst + 3) / 4 * 4;   // whole 16-byte pieces, inside the row stride
+        if (n > 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                             p.scr + ((size_t)bh * p.max_count + t) * p.ns + bfirst),
+                         "r"((uint32_t)n * 4u)
+                         : "memory");
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % G;
     const int first = (yb * W + warp) * R;
     if (first >= N) return;
@@ -370,7 +416,7 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
     const size_t row0 = (size_t)bh * N;
     const size_t lo = sub * S::kBytes;
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB + lo;
-    const float *scr = p.scr + (size_t)bh * p.max_count * N + j;
+    const float *scr = p.scr + (size_t)bh * p.max_count * p.ns + j;
     float2 dq[S::kPairs];
 #pragma unroll
     for (int i = 0; i < S::kPairs; ++i) dq[i] = make_float2(0.f, 0.f);
@@ -387,7 +433,7 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
             const bool in = valid && (unsigned)kk < (unsigned)N;
             kr[u].load(gK + (size_t)(in ? kk : j) * RB);
             // out-of-range entries were never written: select, never multiply
-            wt[u] = in ? scr[(size_t)(t + u) * N] : 0.f;
+            wt[u] = in ? scr[(size_t)(t + u) * p.ns] : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) kr[u].axpy(wt[u], dq);
@@ -397,7 +443,7 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
         const bool in = valid && (unsigned)kk < (unsigned)N;
         S kr;
         kr.load(gK + (size_t)(in ? kk : j) * RB);
-        const float w0 = in ? scr[(size_t)t * N] : 0.f;
+        const float w0 = in ? scr[(size_t)t * p.ns] : 0.f;
         kr.axpy(w0, dq);
     }
     if (!valid) return;
@@ -411,6 +457,18 @@ int stream_lanes() {
 
 // bf16 weights in the forward's P.V update (FIBATT_FLAT_W16=0: fp32
 // weights); measured faster on the 128 x 128 image shape
+// FIBATT_STREAM_PREFETCH: bit mask of the kernels that L2-prefetch their
+// row windows (1 forward, 2 key pass, 4 query pass).  Only the query pass
+// gains (long backward 467.9 -> 455.9 us): its key and dS rows are read once
+// each from DRAM, and the prefetch takes those misses off the warps' path;
+// the forward (156.8 -> 205.7 us) and the key pass (467.9 -> 493.0 us) lose,
+// their extra bulk traffic competing with the loads of a kernel that is
+// already at two thirds of the issue rate.
+int stream_prefetch() {
+    const char *e = getenv("FIBATT_STREAM_PREFETCH");
+    return e ? atoi(e) & 7 : 4;
+}
+
 bool stream_w16() {
     const char *e = getenv("FIBATT_FLAT_W16");
     return !(e && atoi(e) == 0);
@@ -429,6 +487,7 @@ cudaError_t fwd_stream(const FwdArgs &a) {
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
     p.nblk = (tab.N + R * W - 1) / (R * W);
+    p.prefetch = stream_prefetch();
     const size_t smem = sizeof(int) * std::max(1, (int)tab.max_count);
     const cudaError_t e = launch_kernel(fwd_stream_kernel<T, G, W, W16>, dim3((unsigned)((long)a.B * tab.H * p.nblk)),
                                         dim3(W * 32), smem, a.stream, pdl_enabled(), tab, p);
@@ -456,6 +515,8 @@ cudaError_t bwd_stream(const BwdArgs &a) {
     p.scale_log2 = a.scale * kLog2e;
     p.nblk = (tab.N + R * W - 1) / (R * W);
     p.max_count = std::max(1, (int)tab.max_count);
+    p.ns = (tab.N + 31) / 32 * 32;
+    p.prefetch = stream_prefetch();
     const bool pdl = pdl_enabled();
     const size_t smem = sizeof(int) * p.max_count;
     const dim3 block(W * 32);
@@ -498,7 +559,8 @@ cudaError_t launch_bwd_stream(const BwdArgs &a) {
 
 size_t stream_bwd_scratch_bytes(const TableArg &tab, int B) {
     const size_t rows = (size_t)B * tab.H * tab.N;
-    return ((2 * rows + 63) / 64 * 64 + (size_t)B * tab.H * std::max(1, (int)tab.max_count) * tab.N) * sizeof(float);
+    const size_t ns = (tab.N + 31) / 32 * 32;
+    return ((2 * rows + 63) / 64 * 64 + (size_t)B * tab.H * std::max(1, (int)tab.max_count) * ns) * sizeof(float);
 }
 
 }  // namespace fibatt
