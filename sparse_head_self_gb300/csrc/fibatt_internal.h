@@ -141,9 +141,10 @@ cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl);
 cudaError_t launch_fwd_flat(const FwdArgs &a);
 cudaError_t launch_bwd_flat(const BwdArgs &a);       // a.Dws: pair-weight scratch
 size_t flat_bwd_scratch_bytes(const TableArg &tab, int B);
-// Streaming kernels for wide windows (stream.cu): rows 32-byte aligned, no
-// global first token.  The backward's workspace: D_j per row, then dS per
-// (b, h, table entry, query row).
+// Streaming kernels for wide windows (stream.cu): rows 32-byte aligned.  The
+// backward's workspace: (LSE_j log2 e, D_j) per row, then dS per (b, h, table
+// entry, query row); with the global first token the dense row and column
+// kernels (global_token.cu) run around them as around the flat kernels.
 cudaError_t launch_fwd_stream(const FwdArgs &a);
 cudaError_t launch_bwd_stream(const BwdArgs &a);
 size_t stream_bwd_scratch_bytes(const TableArg &tab, int B);

@@ -30,6 +30,7 @@
 
 #include "fibatt_internal.h"
 #include "row_math.cuh"
+#include "row_run.cuh"
 
 namespace fibatt {
 namespace {
@@ -39,102 +40,6 @@ namespace {
 // forward: L2-to-SM bytes 2.80 -> 2.44 GB with 8 warps) but hold fewer warps
 // per SM at these register counts, which costs more: 4 measured fastest.
 constexpr int kStreamWarps = 4;
-
-// 256-bit read-only load and store of eight 32-bit words (32-byte aligned).
-__device__ __forceinline__ void ld8(const uint8_t *p, uint32_t *w) {
-    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
-                   "=r"(w[7])
-                 : "l"(p));
-}
-
-__device__ __forceinline__ void st8(uint8_t *p, const uint32_t *w) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
-// One lane's contiguous slice of a 64-dim row (64/G elements, as 32-bit
-// words: packed bf16 pairs or fp32 values), and the matching fp32
-// accumulator layout (float2 per element pair, in dim order).
-template <typename T, int G>
-struct Run {
-    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    static constexpr int kRowBytes = 64 * (int)sizeof(T);
-    static constexpr int kBytes = kRowBytes / G;    // bytes of the slice: 32 or 64
-    static constexpr int kWords = kBytes / 4;
-    static constexpr int kPairs = 32 / G;           // float2 accumulators
-    static_assert(kBytes % 32 == 0, "a slice is whole 256-bit loads");
-    uint32_t w[kWords];
-
-    __device__ __forceinline__ void load(const uint8_t *p) {
-#pragma unroll
-        for (int i = 0; i < kWords / 8; ++i) ld8(p + 32 * i, w + 8 * i);
-    }
-    // partial dot product over this lane's dims (four sums for ILP)
-    __device__ __forceinline__ float dot(const Run &o) const {
-        float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
-        if constexpr (kBf16) {
-#pragma unroll
-            for (int i = 0; i < kWords; i += 4) {
-                a = dot2_bf16(w[i], o.w[i], a);
-                b = dot2_bf16(w[i + 1], o.w[i + 1], b);
-                c = dot2_bf16(w[i + 2], o.w[i + 2], c);
-                d = dot2_bf16(w[i + 3], o.w[i + 3], d);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kWords; i += 4) {
-                a = fmaf(__uint_as_float(w[i]), __uint_as_float(o.w[i]), a);
-                b = fmaf(__uint_as_float(w[i + 1]), __uint_as_float(o.w[i + 1]), b);
-                c = fmaf(__uint_as_float(w[i + 2]), __uint_as_float(o.w[i + 2]), c);
-                d = fmaf(__uint_as_float(w[i + 3]), __uint_as_float(o.w[i + 3]), d);
-            }
-        }
-        return (a + b) + (c + d);
-    }
-    // acc += p * this (fp32 weight)
-    __device__ __forceinline__ void axpy(float p, float2 (&acc)[kPairs]) const {
-        const float2 pp = make_float2(p, p);
-        if constexpr (kBf16) {
-#pragma unroll
-            for (int i = 0; i < kWords; ++i) acc[i] = fma2(pp, make_float2(bf16_lo(w[i]), bf16_hi(w[i])), acc[i]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < kPairs; ++i)
-                acc[i] = fma2(pp, make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1])), acc[i]);
-        }
-    }
-    // acc += p2 * this for a weight already rounded to bf16 (both halves of
-    // p2); bf16 rows only: one mixed-precision FMA per element
-    __device__ __forceinline__ void axpy_p2(uint32_t p2, float2 (&acc)[kPairs]) const {
-#pragma unroll
-        for (int i = 0; i < kWords; ++i) acc[i] = fma2_bf16(p2, w[i], acc[i]);
-    }
-    // acc * s to the I/O dtype (RNE for bf16), stored at p
-    __device__ __forceinline__ static void store(uint8_t *p, const float2 (&acc)[kPairs], float s) {
-        uint32_t o[kWords];
-        if constexpr (kBf16) {
-#pragma unroll
-            for (int i = 0; i < kWords; ++i) o[i] = pack_bf16x2(acc[i].x * s, acc[i].y * s);
-        } else {
-#pragma unroll
-            for (int i = 0; i < kPairs; ++i) {
-                o[2 * i] = __float_as_uint(acc[i].x * s);
-                o[2 * i + 1] = __float_as_uint(acc[i].y * s);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kWords / 8; ++i) st8(p + 32 * i, o + 8 * i);
-    }
-};
-
-template <int G>
-__device__ __forceinline__ float lanes_sum(float x) {
-#pragma unroll
-    for (int m = 1; m < G; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-    return x;
-}
 
 // Entries [tb, te) of the head's ascending offsets off[0, cnt) that reach a
 // row in [0, N) from at least one of the rows [first, last]: the others are
@@ -151,6 +56,20 @@ __device__ __forceinline__ void trim(const int *off, int cnt, int N, int first, 
     }
     tb = below;
     te = max(tb, cnt - above);
+}
+
+// Global first token: bit i set when the band of row first + i (i < nrows
+// <= 32) reaches position 0, i.e. offset -(first + i) is among off[0, cnt)
+// (the tables are symmetric, so the same bit says whether +(first + i) is).
+// Warp-collective: every lane takes part, whatever its row.
+__device__ __forceinline__ unsigned band_to_zero(const int *off, int cnt, int first, int nrows) {
+    const int lane = threadIdx.x & 31;
+    unsigned hit = 0;
+    for (int t = 0; t < cnt; t += 32) {
+        const int i = t + lane < cnt ? -off[t + lane] - first : -1;
+        hit |= __reduce_or_sync(kFullMask, i >= 0 && i < nrows ? 1u << i : 0u);
+    }
+    return hit;
 }
 
 // Copy of head h's offsets into shared memory; returns the count.
@@ -187,6 +106,7 @@ struct StreamParams {
     float *scr;            // backward: dS per (b, h, table entry, query row), rows of `ns` floats
     int ns;                // scratch row stride (N rounded up to 32: 128-byte rows)
     int prefetch;          // L2 prefetch of the block's row windows: 1 forward, 2 key pass, 4 query pass
+    const float *gw;       // global first token, backward: P_0k, dS_0k per (b, h) ([B*H][2][N])
     float scale, scale_log2;
     int nblk;              // row blocks per (b, h)
     int max_count;         // scratch entries per (b, h)
@@ -197,7 +117,7 @@ constexpr float kMInit = -1.0e30f;
 
 // ------------------------------------------------------------------ forward
 
-template <typename T, int G, int W, bool W16>
+template <typename T, int G, int W, bool W16, bool GT>
 __global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? (24 / W > 0 ? 24 / W : 1) : (16 / W > 0 ? 16 / W : 1))
 fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     using S = Run<T, G>;
@@ -285,7 +205,20 @@ fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
         raise(s0);
         add(va, fast_exp2(s0 - m));
     }
-    if (!valid) return;
+    if constexpr (GT) {
+        // global first token: key 0 for every row j >= 1 whose band misses
+        // it (row 0 itself is the dense row kernel's)
+        const unsigned band0 = band_to_zero(s_off, cnt, first, last - first + 1);
+        const bool need = valid && j >= 1 && !((band0 >> (j - first)) & 1u);
+        S k0r, v0r;
+        k0r.load(gK);
+        v0r.load(gV);
+        float s0 = lanes_sum<G>(q.dot(k0r)) * sl2;
+        s0 = need ? s0 : -INFINITY;
+        raise(s0);
+        add(v0r, fast_exp2(s0 - m));
+    }
+    if (!valid || (GT && j == 0)) return;
     const float ln = (W16 && S::kBf16) ? lt : l;
     S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + sub * S::kBytes, acc, ln > 0.f ? __frcp_rn(ln) : 0.f);
     if (sub == 0) p.LSEout[row0 + j] = l > 0.f ? (m + fast_log2(l)) * kLn2 : -INFINITY;
@@ -313,7 +246,7 @@ __global__ void __launch_bounds__(W * 32) rowdot_stream_kernel(const StreamParam
 
 // Key-centric pass: key row k stationary; the queries attending it are
 // j = k + off[t] (symmetric table), whose pair is query j's entry cnt-1-t.
-template <typename T, int G, int W>
+template <typename T, int G, int W, bool GT>
 __global__ void __launch_bounds__(W * 32)
 bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     using S = Run<T, G>;
@@ -372,14 +305,28 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
         qq.axpy(dS, dk);
         if (in && sub == 0) scr[(ptrdiff_t)j - (ptrdiff_t)t * p.ns] = dS;
     }
-    if (!valid) return;
+    if constexpr (GT) {
+        // global first token: the pair (0, k) for every key k >= 1 whose band
+        // misses query 0, its P and dS from the dense row kernel; dK_0 and
+        // dV_0 are the dense column kernel's
+        const unsigned band0 = band_to_zero(s_off, cnt, first, last - first + 1);
+        const bool need = valid && k >= 1 && !((band0 >> (k - first)) & 1u);
+        const float *gw = p.gw + (size_t)bh * 2 * N;
+        const float P = need ? gw[k] : 0.f, dS = need ? gw[N + k] : 0.f;
+        S q0, g0;
+        q0.load(gQ);
+        g0.load(gG);
+        g0.axpy(P, dv);
+        q0.axpy(dS, dk);
+    }
+    if (!valid || (GT && k == 0)) return;
     S::store(static_cast<uint8_t *>(p.dK) + (row0 + k) * RB + lo, dk, p.scale);
     S::store(static_cast<uint8_t *>(p.dV) + (row0 + k) * RB + lo, dv, 1.f);
 }
 
 // Query-centric pass: dQ_j = scale sum over in-range entries t of
 // dS(j, t) k_{j + off[t]}, dS from the key pass's scratch.
-template <typename T, int G, int W>
+template <typename T, int G, int W, bool GT>
 __global__ void __launch_bounds__(W * 32)
 bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     using S = Run<T, G>;
@@ -446,7 +393,27 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
         const float w0 = in ? scr[(size_t)t * p.ns] : 0.f;
         kr.axpy(w0, dq);
     }
-    if (!valid) return;
+    if constexpr (GT) {
+        // global first token: the pair (j, 0) for every row j >= 1 whose band
+        // misses key 0, P and dS recomputed from the row's own q, dO, LSE and
+        // D; dQ_0 is the dense row kernel's
+        const unsigned band0 = band_to_zero(s_off, cnt, first, last - first + 1);
+        const bool need = valid && j >= 1 && !((band0 >> (j - first)) & 1u);
+        const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB + lo;
+        const uint8_t *gG = static_cast<const uint8_t *>(p.dO) + row0 * RB + lo;
+        const uint8_t *gV = static_cast<const uint8_t *>(p.V) + row0 * RB + lo;
+        S qj, gj, k0r, v0r;
+        qj.load(gQ + (size_t)j * RB);
+        gj.load(gG + (size_t)j * RB);
+        k0r.load(gK);
+        v0r.load(gV);
+        const float2 lj = p.LD[row0 + j];
+        const float s0 = lanes_sum<G>(qj.dot(k0r));
+        const float dp = lanes_sum<G>(gj.dot(v0r));
+        const float P = need ? fast_exp2(fmaf(s0, p.scale_log2, -lj.x)) : 0.f;
+        k0r.axpy(P * (dp - lj.y), dq);
+    }
+    if (!valid || (GT && j == 0)) return;
     S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + lo, dq, p.scale);
 }
 
@@ -474,7 +441,7 @@ bool stream_w16() {
     return !(e && atoi(e) == 0);
 }
 
-template <typename T, int G, bool W16, int W = kStreamWarps>
+template <typename T, int G, bool W16, int W = kStreamWarps, bool GT = false>
 cudaError_t fwd_stream(const FwdArgs &a) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
@@ -489,13 +456,13 @@ cudaError_t fwd_stream(const FwdArgs &a) {
     p.nblk = (tab.N + R * W - 1) / (R * W);
     p.prefetch = stream_prefetch();
     const size_t smem = sizeof(int) * std::max(1, (int)tab.max_count);
-    const cudaError_t e = launch_kernel(fwd_stream_kernel<T, G, W, W16>, dim3((unsigned)((long)a.B * tab.H * p.nblk)),
+    const cudaError_t e = launch_kernel(fwd_stream_kernel<T, G, W, W16, GT>, dim3((unsigned)((long)a.B * tab.H * p.nblk)),
                                         dim3(W * 32), smem, a.stream, pdl_enabled(), tab, p);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <typename T, int G, int W = kStreamWarps>
+template <typename T, int G, int W = kStreamWarps, bool GT = false>
 cudaError_t bwd_stream(const BwdArgs &a) {
     constexpr int R = 32 / G;
     const TableArg &tab = *a.tab;
@@ -517,6 +484,7 @@ cudaError_t bwd_stream(const BwdArgs &a) {
     p.max_count = std::max(1, (int)tab.max_count);
     p.ns = (tab.N + 31) / 32 * 32;
     p.prefetch = stream_prefetch();
+    p.gw = a.gw;
     const bool pdl = pdl_enabled();
     const size_t smem = sizeof(int) * p.max_count;
     const dim3 block(W * 32);
@@ -525,11 +493,11 @@ cudaError_t bwd_stream(const BwdArgs &a) {
     cudaError_t e = launch_kernel(rowdot_stream_kernel<T, G, W>, dim3(row_blocks), block, 0, a.stream, pdl, p, rows);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e == cudaSuccess)
-        e = launch_kernel(bwd_key_stream_kernel<T, G, W>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
+        e = launch_kernel(bwd_key_stream_kernel<T, G, W, GT>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     p.Out = a.dQ;
     if (e == cudaSuccess)
-        e = launch_kernel(bwd_query_stream_kernel<T, G, W>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
+        e = launch_kernel(bwd_query_stream_kernel<T, G, W, GT>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
     count_launches(3);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -544,6 +512,9 @@ int stream_warps() {
 
 cudaError_t launch_fwd_stream(const FwdArgs &a) {
     const bool w16 = stream_w16();
+    if (a.tab->global0)   // the global first token: the default shape only
+        return a.dtype == FIBATT_F32 ? fwd_stream<float, 4, false, kStreamWarps, true>(a)
+                                     : fwd_stream<__nv_bfloat16, 4, true, kStreamWarps, true>(a);
     if (a.dtype == FIBATT_F32) return fwd_stream<float, 4, false>(a);
     if (stream_lanes() == 2)
         return w16 ? fwd_stream<__nv_bfloat16, 2, true>(a) : fwd_stream<__nv_bfloat16, 2, false>(a);
@@ -552,6 +523,9 @@ cudaError_t launch_fwd_stream(const FwdArgs &a) {
 }
 
 cudaError_t launch_bwd_stream(const BwdArgs &a) {
+    if (a.tab->global0)
+        return a.dtype == FIBATT_F32 ? bwd_stream<float, 4, kStreamWarps, true>(a)
+                                     : bwd_stream<__nv_bfloat16, 4, kStreamWarps, true>(a);
     if (a.dtype == FIBATT_F32) return bwd_stream<float, 4>(a);
     if (stream_lanes() == 2) return bwd_stream<__nv_bfloat16, 2>(a);
     return stream_warps() == 8 ? bwd_stream<__nv_bfloat16, 4, 8>(a) : bwd_stream<__nv_bfloat16, 4, 4>(a);

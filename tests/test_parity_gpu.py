@@ -361,7 +361,7 @@ def _global_fwd_bwd(wl, seed, heads_subset=None):
             assert_close_global(f"dV b{b} h{h}", dV[b, h].float().cpu(), rV, wl.dtype)
 
 
-@pytest.mark.parametrize("kernel_path", ["resident", "flat"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["resident", "flat", "flat_legacy"], indirect=True)
 def test_global_token_tiny_fp32(kernel_path):
     _global_fwd_bwd(WORKLOADS["tiny"], 21)
 
@@ -373,7 +373,7 @@ def test_global_token_vitb_shape(name, dtype, kernel_path):
     _global_fwd_bwd(Workload(**{**WORKLOADS[name].__dict__, "B": 2, "dtype": dtype}), 22)
 
 
-@pytest.mark.parametrize("kernel_path", ["resident", "flat", "auto"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["resident", "flat", "flat_legacy", "auto"], indirect=True)
 @pytest.mark.parametrize("N", [1, 2, 3, 9, 40])
 def test_global_token_edge_sizes(N, kernel_path):
     wl = Workload("edge", 2, 3, N, 64, "f32", 1, N, False, True)
@@ -406,7 +406,14 @@ def test_global_token_whole_heads_edge_sizes(N, fuse, monkeypatch):
     _global_fwd_bwd(Workload("edge", 60, 3, N, 64, "f32", 1, N, False, True), 26)
 
 
-def test_global_token_video_two_heads():
+@pytest.mark.parametrize("cluster", ["1", "3", None])
+def test_global_token_video_two_heads(cluster, monkeypatch):
+    # the dense row and column of token 0 split over clusters of 1, 3 or (the
+    # library's choice) 8 CTAs per head
+    if cluster is None:
+        monkeypatch.delenv("FIBATT_GT_CLUSTER", raising=False)
+    else:
+        monkeypatch.setenv("FIBATT_GT_CLUSTER", cluster)
     wl = WORKLOADS["video"].with_batch(1)
     _global_fwd_bwd(wl, 24, heads_subset=(0, wl.H - 1))
 
