@@ -456,7 +456,8 @@ fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
 
     cudaError_t e = cudaSuccess;
     // the resident kernel computes the dense row and column itself when the plan fuses them
-    const bool dense_kernels = a.gw && !(path == BwdPath::Resident && pl.fuse_row0);
+    const bool dense_kernels = a.gw && !(path == BwdPath::Resident && pl.fuse_row0) &&
+                               !(path == BwdPath::Flat && flat_bwd_fuses_global(a));
     if (dense_kernels) e = launch_bwd_global_row(a);   // dQ_0 and the weights of the pairs (0, k)
     if (e == cudaSuccess)
         e = path == BwdPath::Resident ? launch_bwd_resident(a, pl)

@@ -143,9 +143,11 @@ cudaError_t launch_bwd_flat(const BwdArgs &a);       // a.Dws: pair-weight scrat
 size_t flat_bwd_scratch_bytes(const TableArg &tab, int B);
 // Streaming kernels for wide windows (stream.cu): rows 32-byte aligned.  The
 // backward's workspace: (LSE_j log2 e, D_j) per row, then dS per (b, h, table
-// entry, query row); with the global first token the dense row and column
-// kernels (global_token.cu) run around them as around the flat kernels.
+// entry, query row); with the global first token, the dense pairs of row 0
+// and column 0 and per-block sums, all computed inside the streaming kernels
+// (no dense kernel launches).
 cudaError_t launch_fwd_stream(const FwdArgs &a);
+bool flat_bwd_fuses_global(const BwdArgs &a);   // the flat backward computes the dense row and column itself
 cudaError_t launch_bwd_stream(const BwdArgs &a);
 size_t stream_bwd_scratch_bytes(const TableArg &tab, int B);
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);

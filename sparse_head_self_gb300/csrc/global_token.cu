@@ -31,218 +31,26 @@
 #include "fibatt_internal.h"
 #include "row_math.cuh"
 #include "row_run.cuh"
+#include "cluster.cuh"
+#include "dense_row.cuh"
 
 namespace fibatt {
 namespace {
-
-constexpr int kGtG = 4;                  // lanes per row
-constexpr int kGtRows = 32 / kGtG;       // rows per warp step
-
-__device__ __forceinline__ void store_pair(__nv_bfloat16 *row, int i, float2 v) {
-    reinterpret_cast<unsigned int *>(row)[i] = pack_bf16x2(v.x, v.y);
-}
-__device__ __forceinline__ void store_pair(float *row, int i, float2 v) { reinterpret_cast<float2 *>(row)[i] = v; }
-
-// A lane's slice of a row: 256-bit loads when every row pointer is 32-byte
-// aligned (A32), else two 128-bit loads (the boundary only asks for 16).
-template <bool A32, typename S>
-__device__ __forceinline__ void load_slice(S &r, const uint8_t *p) {
-    if constexpr (A32) {
-        r.load(p);
-    } else {
-#pragma unroll
-        for (int i = 0; i < S::kWords / 4; ++i) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p) + i);
-            r.w[4 * i] = v.x;
-            r.w[4 * i + 1] = v.y;
-            r.w[4 * i + 2] = v.z;
-            r.w[4 * i + 3] = v.w;
-        }
-    }
-}
-
-// Sum of acc over the warp's eight row groups (lanes with the same slice);
-// every lane ends with the sum for its slice.
-template <int P>
-__device__ __forceinline__ void groups_sum(float2 (&acc)[P]) {
-#pragma unroll
-    for (int d = kGtG; d < 32; d <<= 1)
-#pragma unroll
-        for (int i = 0; i < P; ++i) {
-            acc[i].x += __shfl_xor_sync(kFullMask, acc[i].x, d);
-            acc[i].y += __shfl_xor_sync(kFullMask, acc[i].y, d);
-        }
-}
-
-// Lanes 0..3 (group 0) write the warp's 64-dim result, float2 index
-// sub * P + i = dims (2 (sub P + i), +1), into dst[32].
-template <int P>
-__device__ __forceinline__ void group0_store(const float2 (&acc)[P], float2 *dst) {
-    const int lane = threadIdx.x & 31;
-    if (lane < kGtG)
-#pragma unroll
-        for (int i = 0; i < P; ++i) dst[lane * P + i] = acc[i];
-}
-
-// ---- thread-block clusters ----------------------------------------------
-
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ unsigned cluster_size() {
-    unsigned n;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-    return n;
-}
-// Every thread of every CTA of the cluster: writes to shared memory before
-// it are visible to the cluster's reads after it.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The address of `p` (this CTA's shared memory) in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_addr(const void *p, unsigned rank) {
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(a)
-                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
-    return a;
-}
-__device__ __forceinline__ float ld_cluster(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ float2 ld_cluster2(uint32_t a) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-    return v;
-}
-
-// Rows [lo, hi) of this CTA's slice of n rows.
-__device__ __forceinline__ void cluster_slice(int n, int &lo, int &hi) {
-    const int c = (int)cluster_size(), r = (int)cluster_rank();
-    const int per = (n + c - 1) / c;
-    lo = min(n, r * per);
-    hi = min(n, lo + per);
-}
-
-// Sum over the cluster's CTAs of the float2 at `mine` (each CTA's partial in
-// its shared memory, lane `lane`'s element), read by CTA 0 in rank order.
-__device__ __forceinline__ float2 cluster_sum2(const float2 *mine) {
-    float2 a = make_float2(0.f, 0.f);
-    for (unsigned r = 0; r < cluster_size(); ++r) {
-        const float2 v = ld_cluster2(cluster_addr(mine, r));
-        a.x += v.x;
-        a.y += v.y;
-    }
-    return a;
-}
 
 template <typename T, int NW, bool A32>
 __global__ void __launch_bounds__(NW * 32)
 fwd_global_row_kernel(int N, long bh0, const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                       float scale_log2, T *__restrict__ O, float *__restrict__ LSE) {
-    using S = Run<T, kGtG>;
-    constexpr int RB = S::kRowBytes, P = S::kPairs;
-    __shared__ float s_m[NW], s_l[NW];
-    __shared__ float2 s_acc[NW][32];
-    __shared__ float c_m, c_l;       // this CTA's state, read by CTA 0 of the cluster
-    __shared__ float2 c_acc[32];
+    __shared__ DenseRowSmem<NW> sm;
     grid_dep_wait();
     grid_dep_launch();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % kGtG, grp = lane / kGtG;
     const size_t bh = (size_t)bh0 + blockIdx.x / cluster_size();
-    const uint8_t *head = reinterpret_cast<const uint8_t *>(Q) + bh * N * RB;
-    const ptrdiff_t dk = reinterpret_cast<const uint8_t *>(K) - reinterpret_cast<const uint8_t *>(Q);
-    const ptrdiff_t dv = reinterpret_cast<const uint8_t *>(V) - reinterpret_cast<const uint8_t *>(Q);
+    const uint8_t *head = reinterpret_cast<const uint8_t *>(Q) + bh * N * Run<T, kGtG>::kRowBytes;
     int kb, ke;
     cluster_slice(N, kb, ke);
-    S q;
-    load_slice<A32>(q, head + sub * S::kBytes);
-    // each row group's own online softmax (log2 units, running maximum raised
-    // only when a score exceeds it by more than 8)
-    float m = -1.0e30f, l = 0.f;
-    float2 acc[P];
-#pragma unroll
-    for (int i = 0; i < P; ++i) acc[i] = make_float2(0.f, 0.f);
-    for (int k0 = kb + warp * kGtRows; k0 < ke; k0 += NW * kGtRows) {
-        const int k = k0 + grp;
-        const bool in = k < ke;
-        const uint8_t *row = head + (size_t)(in ? k : kb) * RB + sub * S::kBytes;
-        S kr, vr;
-        load_slice<A32>(kr, row + dk);
-        load_slice<A32>(vr, row + dv);
-        float s = lanes_sum<kGtG>(q.dot(kr)) * scale_log2;
-        s = in ? s : -INFINITY;
-        if (s > m + 8.f) {
-            const float a = fast_exp2(m - s);
-            l *= a;
-#pragma unroll
-            for (int i = 0; i < P; ++i) acc[i] = mul2(acc[i], make_float2(a, a));
-            m = s;
-        }
-        const float p = fast_exp2(s - m);
-        l += p;
-        vr.axpy(p, acc);
-    }
-    // merge the warp's row groups (every lane takes part)
-#pragma unroll
-    for (int d = kGtG; d < 32; d <<= 1) {
-        const float mo = __shfl_xor_sync(kFullMask, m, d), lo = __shfl_xor_sync(kFullMask, l, d);
-        const float M = fmaxf(m, mo);
-        const float fa = fast_exp2(m - M), fb = fast_exp2(mo - M);
-        l = fa * l + fb * lo;
-#pragma unroll
-        for (int i = 0; i < P; ++i) {
-            const float2 o = make_float2(__shfl_xor_sync(kFullMask, acc[i].x, d), __shfl_xor_sync(kFullMask, acc[i].y, d));
-            acc[i] = make_float2(fa * acc[i].x + fb * o.x, fa * acc[i].y + fb * o.y);
-        }
-        m = M;
-    }
-    group0_store(acc, s_acc[warp]);
-    if (lane == 0) {
-        s_m[warp] = m;
-        s_l[warp] = l;
-    }
-    __syncthreads();
-    if (warp == 0) {   // merge the warps in order, lane L taking dims 2L, 2L + 1
-        float M = -INFINITY;
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
-        float L = 0.f;
-        float2 A = make_float2(0.f, 0.f);
-        for (int w = 0; w < NW; ++w) {
-            const float f = s_l[w] > 0.f ? exp2f(s_m[w] - M) : 0.f;
-            L += f * s_l[w];
-            A.x += f * s_acc[w][lane].x;
-            A.y += f * s_acc[w][lane].y;
-        }
-        c_acc[lane] = A;
-        if (lane == 0) {
-            c_m = M;
-            c_l = L;
-        }
-    }
-    cluster_sync();
-    if (cluster_rank() == 0 && warp == 0) {   // merge the CTAs' states in rank order
-        float M = -INFINITY;
-        for (unsigned r = 0; r < cluster_size(); ++r) M = fmaxf(M, ld_cluster(cluster_addr(&c_m, r)));
-        float L = 0.f;
-        float2 A = make_float2(0.f, 0.f);
-        for (unsigned r = 0; r < cluster_size(); ++r) {
-            const float lr = ld_cluster(cluster_addr(&c_l, r));
-            const float f = lr > 0.f ? exp2f(ld_cluster(cluster_addr(&c_m, r)) - M) : 0.f;
-            const float2 ar = ld_cluster2(cluster_addr(&c_acc[lane], r));
-            L += f * lr;
-            A.x += f * ar.x;
-            A.y += f * ar.y;
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        store_pair(O + bh * N * kHeadDim, lane, make_float2(A.x * inv, A.y * inv));
-        if (lane == 0) LSE[bh * N] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-    }
-    cluster_sync();   // no CTA leaves while CTA 0 reads its shared memory
+    dense_row0_fwd<T, NW, A32>(head, reinterpret_cast<const uint8_t *>(K) - reinterpret_cast<const uint8_t *>(Q),
+                               reinterpret_cast<const uint8_t *>(V) - reinterpret_cast<const uint8_t *>(Q), kb, ke,
+                               scale_log2, O + bh * N * kHeadDim, LSE + bh * N, sm);
 }
 
 // Sum over the warps of s_acc[w][lane] (warp 0), then over the cluster's

@@ -1869,6 +1869,10 @@ static bool use_stream(const TableArg &tab, std::initializer_list<const void *> 
     return true;
 }
 
+bool flat_bwd_fuses_global(const BwdArgs &a) {
+    return a.tab->global0 && use_stream(*a.tab, {a.Q, a.K, a.V, a.O, a.dO, a.dQ, a.dK, a.dV});
+}
+
 cudaError_t launch_bwd_flat(const BwdArgs &a) {
     if (use_stream(*a.tab, {a.Q, a.K, a.V, a.O, a.dO, a.dQ, a.dK, a.dV})) return launch_bwd_stream(a);
     int G = 4;
