@@ -382,6 +382,7 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
         if (sel == PathSel::Resident)
             return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: windows do not fit in shared memory");
         e = launch_fwd_flat(a);
+        if (flat_fwd_fuses_global(a)) row0_from = (long)B * s->impl.tab.H;   // the streaming kernel wrote rows 0
     }
     if (e == cudaSuccess && s->impl.tab.global0 && row0_from < (long)B * s->impl.tab.H)
         e = launch_fwd_global_row(a, row0_from);

@@ -104,8 +104,9 @@ struct DenseRowSmem {
 // raised only when a score exceeds it by more than 8), merged over the
 // cluster; CTA 0 writes O0 and *LSE0.  Every thread of every CTA of the
 // cluster calls it with NW = blockDim.x / 32: it holds a CTA barrier and two
-// cluster barriers.
-template <typename T, int NW, bool A32>
+// cluster barriers.  CLUSTER = false: one CTA computes the whole row (no
+// cluster, warp 0 writes the result after the CTA barrier).
+template <typename T, int NW, bool A32, bool CLUSTER = true>
 __device__ __forceinline__ void dense_row0_fwd(const uint8_t *head, ptrdiff_t dk, ptrdiff_t dv, int kb, int ke,
                                                float scale_log2, T *O0, float *LSE0, DenseRowSmem<NW> &sm) {
     using S = Run<T, kGtG>;
@@ -170,12 +171,19 @@ __device__ __forceinline__ void dense_row0_fwd(const uint8_t *head, ptrdiff_t dk
             A.x += f * sm.acc[w][lane].x;
             A.y += f * sm.acc[w][lane].y;
         }
+        if constexpr (!CLUSTER) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            store_pair(O0, lane, make_float2(A.x * inv, A.y * inv));
+            if (lane == 0) *LSE0 = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+            return;
+        }
         sm.cacc[lane] = A;
         if (lane == 0) {
             sm.cm = M;
             sm.cl = L;
         }
     }
+    if constexpr (!CLUSTER) return;
     cluster_sync();
     if (cluster_rank() == 0 && warp == 0) {   // merge the CTAs' states in rank order
         float M = -INFINITY;

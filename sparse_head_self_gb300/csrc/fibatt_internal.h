@@ -147,9 +147,11 @@ size_t flat_bwd_scratch_bytes(const TableArg &tab, int B);
 // and column 0 and per-block sums, all computed inside the streaming kernels
 // (no dense kernel launches).
 cudaError_t launch_fwd_stream(const FwdArgs &a);
+bool flat_fwd_fuses_global(const FwdArgs &a);   // the flat forward computes the dense row 0 itself
 bool flat_bwd_fuses_global(const BwdArgs &a);   // the flat backward computes the dense row and column itself
 cudaError_t launch_bwd_stream(const BwdArgs &a);
 size_t stream_bwd_scratch_bytes(const TableArg &tab, int B);
+bool stream_row0_in_grid(const TableArg &tab);   // global token: the streaming forward computes the rows 0
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
 

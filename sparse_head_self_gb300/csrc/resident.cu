@@ -1869,6 +1869,10 @@ static bool use_stream(const TableArg &tab, std::initializer_list<const void *> 
     return true;
 }
 
+bool flat_fwd_fuses_global(const FwdArgs &a) {
+    return a.tab->global0 && stream_row0_in_grid(*a.tab) && use_stream(*a.tab, {a.Q, a.K, a.V, a.O});
+}
+
 bool flat_bwd_fuses_global(const BwdArgs &a) {
     return a.tab->global0 && use_stream(*a.tab, {a.Q, a.K, a.V, a.O, a.dO, a.dQ, a.dK, a.dV});
 }

@@ -111,6 +111,8 @@ struct StreamParams {
                            // (row 0's pairs), dS_j0 (column 0's)
     float *part;           // ... per (b, h) and row-pass block: the block's sums of dQ_0, dK_0, dV_0 (3 x 64)
     int nd;                // row-pass blocks per (b, h)
+    int row0_heads;        // global token, forward: blocks ahead of the banded ones computing the dense rows 0
+                           // (B * H), or 0 when the dense row kernel does it
     float scale, scale_log2;
     int nblk;              // row blocks per (b, h)
     int max_count;         // scratch entries per (b, h)
@@ -197,7 +199,7 @@ __device__ __forceinline__ void fwd_stream_rows(const TableArg &tab, const Strea
     }
     if constexpr (GT) {
         // global first token: key 0 for every row j >= 1 whose band misses
-        // it (row 0 itself is the dense row kernel's)
+        // it (row 0 itself is dense: fwd_row0_block)
         const unsigned band0 = band_to_zero(s_off, cnt, first, last - first + 1);
         const bool need = valid && j >= 1 && !((band0 >> (j - first)) & 1u);
         S k0r, v0r;
@@ -214,6 +216,22 @@ __device__ __forceinline__ void fwd_stream_rows(const TableArg &tab, const Strea
     if (sub == 0) p.LSEout[row0 + j] = l > 0.f ? (m + fast_log2(l)) * kLn2 : -INFINITY;
 }
 
+// Global first token: the dense row 0 of head blockIdx.x, one block per
+// head over every key.  Launched ahead of the banded blocks in the same
+// grid (fwd_stream_kernel takes blocks past the heads), so these longer
+// blocks start first and run beside the banded ones.
+template <typename T, int W>
+__device__ __forceinline__ void fwd_row0_block(const TableArg &tab, const StreamParams &p, int bh) {
+    constexpr int RB = Run<T, 4>::kRowBytes;
+    __shared__ DenseRowSmem<W> sm;
+    const int N = tab.N;
+    const uint8_t *head = static_cast<const uint8_t *>(p.Q) + (size_t)bh * N * RB;
+    dense_row0_fwd<T, W, true, false>(head, static_cast<const uint8_t *>(p.K) - static_cast<const uint8_t *>(p.Q),
+                                      static_cast<const uint8_t *>(p.V) - static_cast<const uint8_t *>(p.Q), 0, N,
+                                      p.scale_log2, static_cast<T *>(p.Out) + (size_t)bh * N * kHeadDim,
+                                      p.LSEout + (size_t)bh * N, sm);
+}
+
 template <typename T, int G, int W, bool W16, bool GT>
 __global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? (24 / W > 0 ? 24 / W : 1) : (16 / W > 0 ? 16 / W : 1))
 fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
@@ -221,7 +239,17 @@ fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     constexpr int RB = Run<T, G>::kRowBytes;
     extern __shared__ int s_off[];
     const int N = tab.N;
-    const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
+    int b = (int)blockIdx.x;
+    if constexpr (GT) {   // the first B*H blocks: the dense rows 0 (fwd_row0_block), when in this grid
+        if (b < p.row0_heads) {
+            grid_dep_wait();
+            grid_dep_launch();
+            fwd_row0_block<T, W>(tab, p, b);
+            return;
+        }
+        b -= p.row0_heads;
+    }
+    const int bh = b / p.nblk, yb = b % p.nblk;
     const int cnt = load_offsets(tab, bh % tab.H, s_off);
     if (p.prefetch & 1) {   // Q, K and V are inputs: their rows may be prefetched into L2 while
         // the previous kernel drains (L2 is the point of coherence, so the
@@ -544,6 +572,19 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
     S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + lo, dq, p.scale);
 }
 
+}  // namespace
+
+// Global first token: the streaming forward computes the dense rows 0 in
+// blocks of its own grid (one block of kStreamWarps warps per head, over
+// every key) while they take little longer than the banded blocks; for long
+// sequences one block per head would outlast the whole banded grid (128 x
+// 128 image shape, 16385 keys: forward 336 us against 193 us with the
+// cluster kernel of global_token.cu), so there the dense row kernel runs.
+// Video shape (1569 keys): forward 49.3 -> 39.9 us.
+bool stream_row0_in_grid(const TableArg &tab) { return tab.N <= 4096; }
+
+namespace {
+
 int stream_lanes() {
     const char *e = getenv("FIBATT_FLAT_LANES");
     return (e && atoi(e) == 2) ? 2 : 4;
@@ -582,9 +623,11 @@ cudaError_t fwd_stream(const FwdArgs &a) {
     p.scale_log2 = a.scale * kLog2e;
     p.nblk = (tab.N + R * W - 1) / (R * W);
     p.prefetch = stream_prefetch();
+    p.row0_heads = GT && stream_row0_in_grid(tab) ? a.B * tab.H : 0;
     const size_t smem = sizeof(int) * std::max(1, (int)tab.max_count);
-    const cudaError_t e = launch_kernel(fwd_stream_kernel<T, G, W, W16, GT>, dim3((unsigned)((long)a.B * tab.H * p.nblk)),
-                                        dim3(W * 32), smem, a.stream, pdl_enabled(), tab, p);
+    const long blocks = (long)a.B * tab.H * p.nblk + p.row0_heads;   // the dense row-0 blocks first
+    const cudaError_t e = launch_kernel(fwd_stream_kernel<T, G, W, W16, GT>, dim3((unsigned)blocks), dim3(W * 32), smem,
+                                        a.stream, pdl_enabled(), tab, p);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -418,6 +418,14 @@ def test_global_token_video_two_heads(cluster, monkeypatch):
     _global_fwd_bwd(wl, 24, heads_subset=(0, wl.H - 1))
 
 
+@pytest.mark.parametrize("kernel_path", ["flat", "flat_legacy"], indirect=True)
+def test_global_token_long_rows(kernel_path):
+    # 5000 tokens: beyond the length at which the streaming forward computes
+    # the dense row 0 in its own grid, so the dense row kernel takes it
+    wl = Workload("gt_long", 1, 2, 5000, 64, "bf16", 64, 5000, True, True)
+    _global_fwd_bwd(wl, 25)
+
+
 def test_global_token_only_support_gives_v0():
     # no distances, no diagonal: every query but token 0 attends key 0 alone
     N, B = 50, 2
