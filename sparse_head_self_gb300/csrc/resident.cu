@@ -1646,14 +1646,16 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     // partial-state slot per stage; and it keeps the last wave's units whole,
     // so it is taken when that wave is empty or at least a quarter full (a
     // few whole units in a last wave cost more than the separate row kernel
-    // with last-wave pieces).
+    // with last-wave pieces), or when there are many waves, the row kernel's
+    // cost growing with the heads (B = 256, ViT-B shape, 20.2 waves: fused
+    // 112.0 us against 123.6 us; B = 64, 5.05 waves: 33.6 against 32.5 us).
     bool staged_all = true;
     for (int h = 0; h < tab.H; ++h) staged_all = staged_all && tab.start[h + 1] > tab.start[h];
     pl->fuse_row0 = tab.global0 && qsplit == 1 && staged_all;
     if (const char *e = getenv("FIBATT_GT_FUSE"))   // 0: never, else whenever possible
         pl->fuse_row0 = pl->fuse_row0 && atoi(e) != 0;
     else
-        pl->fuse_row0 = pl->fuse_row0 && (left == 0 || 4 * left >= pl->grid);
+        pl->fuse_row0 = pl->fuse_row0 && (left == 0 || 4 * left >= pl->grid || units >= 8L * pl->grid);
     const size_t slot_bytes = (size_t)gwarps * 33 * sizeof(float2);   // one partial slot per stage
     if (pl->fuse_row0)
         while (stages > 2 && (stage + slot_bytes) * stages > budget) pl->stages = --stages;

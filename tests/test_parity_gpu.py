@@ -396,6 +396,14 @@ def test_global_token_whole_heads(name, dtype, B, fuse, monkeypatch):
     _global_fwd_bwd(Workload(**{**WORKLOADS[name].__dict__, "B": B, "dtype": dtype}), 25)
 
 
+def test_global_token_many_waves():
+    # B = 104 (1248 whole-head units, 8.2 waves with a last wave of 32): row 0
+    # computed inside the resident forward because of the number of waves;
+    # heads 0 and 11 of every batch element compared
+    wl = Workload(**{**WORKLOADS["vitb"].__dict__, "B": 104})
+    _global_fwd_bwd(wl, 26, heads_subset=(0, wl.H - 1))
+
+
 @pytest.mark.parametrize("fuse", ["1", "0"])
 @pytest.mark.parametrize("N", [1, 2, 9, 40])
 def test_global_token_whole_heads_edge_sizes(N, fuse, monkeypatch):
