@@ -107,12 +107,9 @@ struct StreamParams {
     float *scr;            // backward: dS per (b, h, table entry, query row), rows of `ns` floats
     int ns;                // scratch row stride (N rounded up to 32: 128-byte rows)
     int prefetch;          // L2 prefetch of the block's row windows: 1 forward, 2 key pass, 4 query pass
-    float *gw;             // global first token, backward: per (b, h) three rows of `ns` floats: P_0k and dS_0k
-                           // (row 0's pairs), dS_j0 (column 0's)
-    float *part;           // ... per (b, h) and row-pass block: the block's sums of dQ_0, dK_0, dV_0 (3 x 64)
-    int nd;                // row-pass blocks per (b, h)
-    int row0_heads;        // global token, forward: blocks ahead of the banded ones computing the dense rows 0
-                           // (B * H), or 0 when the dense row kernel does it
+    float *gw;             // global first token, backward: dS_j0 of column 0, a row of `ns` floats per (b, h)
+    int row0_heads;        // global token: B * H when the dense blocks (forward: rows 0; key pass: dQ_0 and
+                           // column 0) run in the kernel's own grid ahead of the banded blocks, else 0
     float scale, scale_log2;
     int nblk;              // row blocks per (b, h)
     int max_count;         // scratch entries per (b, h)
@@ -285,89 +282,93 @@ __global__ void __launch_bounds__(W * 32) rowdot_stream_kernel(const StreamParam
     if (r < rows && sub == 0) p.LD[r] = make_float2(l * kLog2e, d);
 }
 
-// Row pass with the global first token (G = 4 lanes per row, head-major
-// blocks of kGtDotWarps warps x kGtDotSteps steps of 8 rows): per row j,
-// besides (LSE_j log2 e, D_j), the two dense pairs the row takes part in --
-// (0, j) of row 0: P_0j and dS_0j into gw (the key pass's), dS_0j k_j into the
-// block's sum of dQ_0; (j, 0) of column 0: dS_j0 into gw (the query pass's),
-// dS_j0 q_j and P_j0 dO_j into the block's sums of dK_0 and dV_0 -- and the
-// block's three sums into `part` (added up by the key and query passes).
-constexpr int kGtDotWarps = 8, kGtDotSteps = 4;
-constexpr int kGtDotRows = kGtDotWarps * 8 * kGtDotSteps;
-
-template <typename T>
-__global__ void __launch_bounds__(kGtDotWarps * 32)
-rowdot_global_kernel(const StreamParams p, int N) {
+// Global first token, key pass: the dense parts of row 0 and column 0, one
+// block per head each, placed ahead of the banded blocks in the key pass's
+// grid so that they start first and run beside them.  Four lanes per row,
+// eight rows per warp step; the warps' sums merged in shared memory in warp
+// order.
+//   dense_dq0_block: dQ_0 = scale sum over every key k of dS_0k k_k.
+//   dense_col_block: for every query j, dS_j0 (into gw, for the query pass),
+//                    dK_0 = scale sum dS_j0 q_j and dV_0 = sum P_j0 dO_j.
+template <typename T, int W>
+__device__ __forceinline__ void dense_dq0_block(const TableArg &tab, const StreamParams &p, int bh) {
     using S = Run<T, 4>;
     constexpr int RB = S::kRowBytes, P = S::kPairs;
-    __shared__ float2 s_sum[3][kGtDotWarps][32];
-    grid_dep_wait();
-    grid_dep_launch();
+    __shared__ float2 s_sum[W][32];
+    const int N = tab.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % 4, grp = lane / 4;
-    const int bh = blockIdx.x / p.nd, yb = blockIdx.x % p.nd;
     const size_t row0 = (size_t)bh * N, lo = sub * S::kBytes;
-    const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB + lo;
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB + lo;
     const uint8_t *gV = static_cast<const uint8_t *>(p.V) + row0 * RB + lo;
-    const uint8_t *gO = static_cast<const uint8_t *>(p.O) + row0 * RB + lo;
-    const uint8_t *gG = static_cast<const uint8_t *>(p.dO) + row0 * RB + lo;
-    float *gw = p.gw + (size_t)bh * 3 * p.ns;
-    // row 0's query, dO and O, and key and value row 0
-    S q0, g0, k0, v0;
-    q0.load(gQ);
-    g0.load(gG);
-    k0.load(gK);
-    v0.load(gV);
-    float D0;
-    {
-        S o0;
-        o0.load(gO);
-        D0 = lanes_sum<4>(g0.dot(o0));
-    }
-    const float l20 = p.LSE[row0] * kLog2e, sl2 = p.scale_log2;
-    float2 dq[P], dk[P], dv[P];
+    S q0, g0;
+    q0.load(static_cast<const uint8_t *>(p.Q) + row0 * RB + lo);
+    g0.load(static_cast<const uint8_t *>(p.dO) + row0 * RB + lo);
+    const float2 l0 = p.LD[row0];
+    float2 dq[P];
 #pragma unroll
-    for (int i = 0; i < P; ++i) dq[i] = dk[i] = dv[i] = make_float2(0.f, 0.f);
-    for (int st = 0; st < kGtDotSteps; ++st) {
-        const int j = yb * kGtDotRows + (st * kGtDotWarps + warp) * 8 + grp;
-        const bool in = j < N;
-        const size_t r = (size_t)(in ? j : 0) * RB;
-        S qj, kj, vj, oj, gj;
-        qj.load(gQ + r);
-        kj.load(gK + r);
-        vj.load(gV + r);
-        oj.load(gO + r);
-        gj.load(gG + r);
-        const float l2 = p.LSE[row0 + (in ? j : 0)] * kLog2e;
-        const float Dj = lanes_sum<4>(gj.dot(oj));
-        // (0, j): row 0's pair with key j
-        const float s0 = lanes_sum<4>(q0.dot(kj)), dp0 = lanes_sum<4>(g0.dot(vj));
-        const float P0 = in ? fast_exp2(fmaf(s0, sl2, -l20)) : 0.f, dS0 = P0 * (dp0 - D0);
-        kj.axpy(dS0, dq);
-        // (j, 0): row j's pair with key 0
-        const float s1 = lanes_sum<4>(qj.dot(k0)), dp1 = lanes_sum<4>(gj.dot(v0));
-        const float P1 = in ? fast_exp2(fmaf(s1, sl2, -l2)) : 0.f, dS1 = P1 * (dp1 - Dj);
-        qj.axpy(dS1, dk);
-        gj.axpy(P1, dv);
-        if (in && sub == 0) {
-            p.LD[row0 + j] = make_float2(l2, Dj);
-            gw[j] = P0;
-            gw[p.ns + j] = dS0;
-            gw[2 * p.ns + j] = dS1;
-        }
+    for (int i = 0; i < P; ++i) dq[i] = make_float2(0.f, 0.f);
+    for (int k0 = warp * 8; k0 < N; k0 += W * 8) {
+        const int k = k0 + grp;
+        const bool in = k < N;
+        const size_t r = (size_t)(in ? k : 0) * RB;
+        S kr, vr;
+        kr.load(gK + r);
+        vr.load(gV + r);
+        const float sc = lanes_sum<4>(q0.dot(kr)), dp = lanes_sum<4>(g0.dot(vr));
+        const float P0 = in ? fast_exp2(fmaf(sc, p.scale_log2, -l0.x)) : 0.f;
+        kr.axpy(P0 * (dp - l0.y), dq);
     }
-    // the block's sums, over row groups, then warps in order
     groups_sum(dq);
+    group0_store(dq, s_sum[warp]);
+    __syncthreads();
+    if (warp == 0) {
+        float2 a = make_float2(0.f, 0.f);
+        for (int w = 0; w < W; ++w) a = add2(a, s_sum[w][lane]);
+        store_pair(static_cast<T *>(p.Out) + row0 * kHeadDim, lane, make_float2(a.x * p.scale, a.y * p.scale));
+    }
+}
+
+template <typename T, int W>
+__device__ __forceinline__ void dense_col_block(const TableArg &tab, const StreamParams &p, int bh) {
+    using S = Run<T, 4>;
+    constexpr int RB = S::kRowBytes, P = S::kPairs;
+    __shared__ float2 s_sum[2][W][32];
+    const int N = tab.N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = lane % 4, grp = lane / 4;
+    const size_t row0 = (size_t)bh * N, lo = sub * S::kBytes;
+    const uint8_t *gQ = static_cast<const uint8_t *>(p.Q) + row0 * RB + lo;
+    const uint8_t *gG = static_cast<const uint8_t *>(p.dO) + row0 * RB + lo;
+    float *gw = p.gw + (size_t)bh * p.ns;
+    S k0r, v0r;
+    k0r.load(static_cast<const uint8_t *>(p.K) + row0 * RB + lo);
+    v0r.load(static_cast<const uint8_t *>(p.V) + row0 * RB + lo);
+    float2 dk[P], dv[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) dk[i] = dv[i] = make_float2(0.f, 0.f);
+    for (int j0 = warp * 8; j0 < N; j0 += W * 8) {
+        const int j = j0 + grp;
+        const bool in = j < N;
+        const int jc = in ? j : 0;
+        S qj, gj;
+        qj.load(gQ + (size_t)jc * RB);
+        gj.load(gG + (size_t)jc * RB);
+        const float2 lj = p.LD[row0 + jc];
+        const float sc = lanes_sum<4>(qj.dot(k0r)), dp = lanes_sum<4>(gj.dot(v0r));
+        const float Pj = in ? fast_exp2(fmaf(sc, p.scale_log2, -lj.x)) : 0.f, dS = Pj * (dp - lj.y);
+        if (in && sub == 0) gw[j] = dS;
+        qj.axpy(dS, dk);
+        gj.axpy(Pj, dv);
+    }
     groups_sum(dk);
     groups_sum(dv);
-    group0_store(dq, s_sum[0][warp]);
-    group0_store(dk, s_sum[1][warp]);
-    group0_store(dv, s_sum[2][warp]);
+    group0_store(dk, s_sum[0][warp]);
+    group0_store(dv, s_sum[1][warp]);
     __syncthreads();
-    if (warp < 3) {
+    if (warp < 2) {
         float2 a = make_float2(0.f, 0.f);
-        for (int w = 0; w < kGtDotWarps; ++w) a = add2(a, s_sum[warp][w][lane]);
-        reinterpret_cast<float2 *>(p.part)[((size_t)bh * p.nd + yb) * 96 + warp * 32 + lane] = a;
+        for (int w = 0; w < W; ++w) a = add2(a, s_sum[warp][w][lane]);
+        const float sc = warp == 0 ? p.scale : 1.f;
+        store_pair(static_cast<T *>(warp == 0 ? p.dK : p.dV) + row0 * kHeadDim, lane, make_float2(a.x * sc, a.y * sc));
     }
 }
 
@@ -420,33 +421,18 @@ __device__ __forceinline__ void key_rows(const TableArg &tab, const StreamParams
     }
     if constexpr (GT) {
         // global first token: the pair (0, k) for every key k >= 1 whose band
-        // misses query 0, its P and dS from the row pass; key 0's whole
-        // column is dense: dK_0 and dV_0 are the sums of the row pass's
-        // blocks, added here in block order
+        // misses query 0, computed here from the key and value rows already
+        // in registers; key 0's whole column is the dense column block's
         const unsigned band0 = band_to_zero(s_off, cnt, first, last - first + 1);
         const bool need = valid && k >= 1 && !((band0 >> (k - first)) & 1u);
-        const float *gw = p.gw + (size_t)bh * 3 * p.ns;
-        const float P = need ? gw[k] : 0.f, dS = need ? gw[p.ns + k] : 0.f;
         S q0, g0;
         q0.load(gQ);
         g0.load(gG);
-        g0.axpy(P, dv);
-        q0.axpy(dS, dk);
-        if (k == 0 && valid) {
-            const float2 *part = reinterpret_cast<const float2 *>(p.part) + (size_t)bh * p.nd * 96;
-            float2 sk[S::kPairs], sv[S::kPairs];
-#pragma unroll
-            for (int i = 0; i < S::kPairs; ++i) sk[i] = sv[i] = make_float2(0.f, 0.f);
-#pragma unroll 4
-            for (int d = 0; d < p.nd; ++d)
-#pragma unroll
-                for (int i = 0; i < S::kPairs; ++i) {
-                    sk[i] = add2(sk[i], part[(size_t)d * 96 + 32 + sub * S::kPairs + i]);
-                    sv[i] = add2(sv[i], part[(size_t)d * 96 + 64 + sub * S::kPairs + i]);
-                }
-            S::store(static_cast<uint8_t *>(p.dK) + row0 * RB + lo, sk, p.scale);
-            S::store(static_cast<uint8_t *>(p.dV) + row0 * RB + lo, sv, 1.f);
-        }
+        const float2 l0 = ld[0];
+        const float s0 = lanes_sum<G>(q0.dot(kk)), dp0 = lanes_sum<G>(g0.dot(vv));
+        const float P0 = need ? fast_exp2(fmaf(s0, sl2, -l0.x)) : 0.f;
+        g0.axpy(P0, dv);
+        q0.axpy(P0 * (dp0 - l0.y), dk);
     }
     if (!valid || (GT && k == 0)) return;
     S::store(static_cast<uint8_t *>(p.dK) + (row0 + k) * RB + lo, dk, p.scale);
@@ -463,7 +449,20 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
     constexpr int RB = S::kRowBytes;
     extern __shared__ int s_off[];
     const int N = tab.N;
-    const int bh = blockIdx.x / p.nblk, yb = blockIdx.x % p.nblk;
+    int b = (int)blockIdx.x;
+    if constexpr (GT) {   // the first 2 B H blocks: row 0's dQ_0, then column 0 (dense_*_block)
+        if (b < 2 * p.row0_heads) {
+            grid_dep_wait();
+            grid_dep_launch();
+            if (b < p.row0_heads)
+                dense_dq0_block<T, W>(tab, p, b);
+            else
+                dense_col_block<T, W>(tab, p, b - p.row0_heads);
+            return;
+        }
+        b -= 2 * p.row0_heads;
+    }
+    const int bh = b / p.nblk, yb = b % p.nblk;
     const int cnt = load_offsets(tab, bh % tab.H, s_off);
     if (p.prefetch & 2) {   // the query and dO rows are inputs (see the forward)
         const size_t head = (size_t)bh * N * RB;
@@ -548,25 +547,14 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
     }
     if constexpr (GT) {
         // global first token: the pair (j, 0) for every row j >= 1 whose band
-        // misses key 0, its dS from the row pass; row 0 is dense: dQ_0 is the
-        // sum of the row pass's blocks, added here in block order
+        // misses key 0, its dS from the key pass's dense column block; row 0
+        // is dense: its dQ_0 is the dense dQ_0 block's
         const unsigned band0 = band_to_zero(s_off, cnt, first, last - first + 1);
         const bool need = valid && j >= 1 && !((band0 >> (j - first)) & 1u);
-        const float dS = need ? p.gw[(size_t)bh * 3 * p.ns + 2 * p.ns + j] : 0.f;
+        const float dS = need ? p.gw[(size_t)bh * p.ns + j] : 0.f;
         S k0r;
         k0r.load(gK);
         k0r.axpy(dS, dq);
-        if (j == 0 && valid) {
-            const float2 *part = reinterpret_cast<const float2 *>(p.part) + (size_t)bh * p.nd * 96;
-            float2 sq[S::kPairs];
-#pragma unroll
-            for (int i = 0; i < S::kPairs; ++i) sq[i] = make_float2(0.f, 0.f);
-#pragma unroll 4
-            for (int d = 0; d < p.nd; ++d)
-#pragma unroll
-                for (int i = 0; i < S::kPairs; ++i) sq[i] = add2(sq[i], part[(size_t)d * 96 + sub * S::kPairs + i]);
-            S::store(static_cast<uint8_t *>(p.Out) + row0 * RB + lo, sq, p.scale);
-        }
     }
     if (!valid || (GT && j == 0)) return;
     S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + lo, dq, p.scale);
@@ -656,22 +644,18 @@ cudaError_t bwd_stream(const BwdArgs &a) {
     p.prefetch = stream_prefetch();
     const size_t heads = (size_t)a.B * tab.H;
     p.gw = p.scr + heads * p.max_count * p.ns;   // global token: after the scratch
-    p.nd = (tab.N + kGtDotRows - 1) / kGtDotRows;
-    p.part = p.gw + heads * 3 * p.ns;
+    p.row0_heads = GT ? (int)heads : 0;
     const bool pdl = pdl_enabled();
     const size_t smem = sizeof(int) * p.max_count;
     const dim3 block(W * 32);
     const unsigned row_blocks = (unsigned)((rows + R * W - 1) / (R * W));
     const unsigned blocks = (unsigned)((long)a.B * tab.H * p.nblk);
-    cudaError_t e;
-    if constexpr (GT)
-        e = launch_kernel(rowdot_global_kernel<T>, dim3((unsigned)(heads * p.nd)), dim3(kGtDotWarps * 32), 0, a.stream,
-                          pdl, p, (int)tab.N);
-    else
-        e = launch_kernel(rowdot_stream_kernel<T, G, W>, dim3(row_blocks), block, 0, a.stream, pdl, p, rows);
+    cudaError_t e = launch_kernel(rowdot_stream_kernel<T, G, W>, dim3(row_blocks), block, 0, a.stream, pdl, p, rows);
     if (e == cudaSuccess) e = cudaGetLastError();
+    p.Out = a.dQ;   // the key pass's dense dQ_0 blocks write row 0 of dQ
     if (e == cudaSuccess)
-        e = launch_kernel(bwd_key_stream_kernel<T, G, W, GT>, dim3(blocks), block, smem, a.stream, pdl, tab, p);
+        e = launch_kernel(bwd_key_stream_kernel<T, G, W, GT>, dim3(blocks + 2 * (unsigned)p.row0_heads), block, smem,
+                          a.stream, pdl, tab, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     p.Out = a.dQ;
     if (e == cudaSuccess)
@@ -713,8 +697,7 @@ size_t stream_bwd_scratch_bytes(const TableArg &tab, int B) {
     const size_t rows = (size_t)B * tab.H * tab.N, heads = (size_t)B * tab.H;
     const size_t ns = (tab.N + 31) / 32 * 32;
     size_t floats = (2 * rows + 63) / 64 * 64 + heads * std::max(1, (int)tab.max_count) * ns;
-    if (tab.global0)   // the global token's pair weights and the row pass's block sums
-        floats += heads * (3 * ns + ((tab.N + kGtDotRows - 1) / kGtDotRows) * 192);
+    if (tab.global0) floats += heads * ns;   // the global token's column weights dS_j0
     return floats * sizeof(float);
 }
 
