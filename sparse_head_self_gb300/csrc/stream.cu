@@ -36,6 +36,13 @@
 namespace fibatt {
 namespace {
 
+// Register budgets (bf16): the forward at 64 registers (32 warps per SM;
+// video 36.7 -> 34.4 us, 128 x 128 image 156.4 -> 149.8 us against its own
+// choice of 78; 48 registers spill: 43.4 / 184.3 us), the key pass at 80 (24
+// warps; 100.2 -> 98.2 and 444.0 -> 429.8 us against 94; 64 spill: 136.0 /
+// 626.2 us); with the global token the key pass takes 96 (20 warps; 80
+// spill: 128 x 128 image 539 -> 582 us).
+//
 // Warps per block (consecutive row groups of one head).  Larger blocks
 // raise the L1 hits between neighbouring offsets (the 128 x 128 image shape's
 // forward: L2-to-SM bytes 2.80 -> 2.44 GB with 8 warps) but hold fewer warps
@@ -230,7 +237,7 @@ __device__ __forceinline__ void fwd_row0_block(const TableArg &tab, const Stream
 }
 
 template <typename T, int G, int W, bool W16, bool GT>
-__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? (24 / W > 0 ? 24 / W : 1) : (16 / W > 0 ? 16 / W : 1))
+__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? (32 / W > 0 ? 32 / W : 1) : (16 / W > 0 ? 16 / W : 1))
 fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     constexpr int R = 32 / G;
     constexpr int RB = Run<T, G>::kRowBytes;
@@ -442,7 +449,7 @@ __device__ __forceinline__ void key_rows(const TableArg &tab, const StreamParams
 // Key-centric pass: key row k stationary; the queries attending it are
 // j = k + off[t] (symmetric table), whose pair is query j's entry cnt-1-t.
 template <typename T, int G, int W, bool GT>
-__global__ void __launch_bounds__(W * 32)
+__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? ((GT ? 20 : 24) / W > 0 ? (GT ? 20 : 24) / W : 1) : 1)
 bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     using S = Run<T, G>;
     constexpr int R = 32 / G;
