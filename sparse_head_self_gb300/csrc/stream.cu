@@ -41,7 +41,8 @@ namespace {
 // choice of 78; 48 registers spill: 43.4 / 184.3 us), the key pass at 80 (24
 // warps; 100.2 -> 98.2 and 444.0 -> 429.8 us against 94; 64 spill: 136.0 /
 // 626.2 us); with the global token the key pass takes 96 (20 warps; 80
-// spill: 128 x 128 image 539 -> 582 us).
+// spill: 128 x 128 image 539 -> 582 us); the query pass 48 (40 warps; 97.4 ->
+// 95.0 and 428.1 -> 413.2 us against 52; 40 spill: 96.9 / 421.5 us).
 //
 // Warps per block (consecutive row groups of one head).  Larger blocks
 // raise the L1 hits between neighbouring offsets (the 128 x 128 image shape's
@@ -486,7 +487,7 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
 // Query-centric pass: dQ_j = scale sum over in-range entries t of
 // dS(j, t) k_{j + off[t]}, dS from the key pass's scratch.
 template <typename T, int G, int W, bool GT>
-__global__ void __launch_bounds__(W * 32)
+__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? (40 / W > 0 ? 40 / W : 1) : 1)
 bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     using S = Run<T, G>;
     constexpr int R = 32 / G;
