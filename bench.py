@@ -166,6 +166,8 @@ def recorded_traffic(kernel: str, workload: str):
         wr = max(int(ent["dram_write"]), int(ent["l2_write"]))
         out = {"read": rd, "write": wr, "total": rd + wr, "dram_write": int(ent["dram_write"]),
                "l2_write": int(ent["l2_write"]), "capture": ent.get("capture")}
+        if "l2_to_sm_read" in ent:   # reads that missed L1 (l1tex__m_xbar2l1tex_read_bytes.sum)
+            out["l2_to_sm_read"] = int(ent["l2_to_sm_read"])
         if "scaled_from" in ent:
             out["scaled_from"] = ent["scaled_from"]
         return out
@@ -567,6 +569,8 @@ def gb300_arm(args):
     d = head_rec[dominant]
     kname = f"fibatt_{dominant}"
     traffic = recorded_traffic(kname, wl.name)
+    if traffic is not None and "l2_to_sm_read" in traffic:
+        traffic["l2_to_sm_GB_s"] = round(traffic["l2_to_sm_read"] / d["ms"] / 1e6, 1)   # at the bench's time
     hbm_line = {"bound": "hbm", "kernel": kname, "achieved": d["GB_s"], "peak": peak, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": d["frac_hbm"], "traffic": None if traffic is None else traffic["total"],
                 "traffic_detail": traffic, "algorithmic_bytes": d["algorithmic_bytes"], "avg_ms": d["ms"]}
