@@ -154,6 +154,7 @@ size_t stream_bwd_scratch_bytes(const TableArg &tab, int B);
 bool stream_row0_in_grid(const TableArg &tab);   // global token: the streaming forward computes the rows 0
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
+cudaError_t read_stream_device_error(unsigned *code, bool clear);   // stream.cu's copy of the word
 
 // Global first token (global_token.cu): the dense row of token 0 (forward,
 // after the banded kernel), its dense row before the banded backward, and

@@ -1936,8 +1936,11 @@ cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
 
 // Read (and optionally clear) the device error word of the current device.
 cudaError_t read_device_error(unsigned *code, bool clear) {
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned));
-    if (e != cudaSuccess || !clear || *code == 0) return e;
+    unsigned mine = 0, other = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&mine, g_device_error, sizeof(unsigned));
+    if (e == cudaSuccess) e = read_stream_device_error(&other, clear);   // the streaming kernels' word
+    *code = mine | other;
+    if (e != cudaSuccess || !clear || mine == 0) return e;
     const unsigned zero = 0;
     return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
 }

@@ -28,10 +28,13 @@
 #include <cstdlib>
 #include <type_traits>
 
+#include <cuda.h>
+
 #include "fibatt_internal.h"
 #include "row_math.cuh"
 #include "row_run.cuh"
 #include "dense_row.cuh"
+#include "tma_common.cuh"
 
 namespace fibatt {
 namespace {
@@ -268,6 +271,238 @@ fwd_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     grid_dep_launch();
     const int first = (yb * W + (int)(threadIdx.x >> 5)) * R;
     if (first < N) fwd_stream_rows<T, G, W16, GT>(tab, p, s_off, cnt, bh, first);   // whole warps
+}
+
+// ----------------------------------------------- forward, near window staged
+//
+// The table entries with |off| <= dmax reach, from a block of Tq = 8W query
+// rows j0 .. j0 + Tq - 1, the key rows j0 + off[nb] .. j0 + Tq - 1 +
+// off[ne - 1]: at most Tq + 2 dmax rows, shared by every near entry (the
+// small Fibonacci distances lie within a few dozen rows of each other).  The
+// block stages that window of K and V once in shared memory with bulk tensor
+// copies (boxes of kWinBox rows, 128-byte swizzle), computes its far entries
+// from global memory as fwd_stream_rows does while the copies land, then the
+// near ones from the window.  The far entries read every key row once per
+// pair either way; the near ones read a staged row once per block instead of
+// once per pair.
+
+constexpr int kWinRows = 256;                        // staged key (and value) rows per block
+constexpr int kWinBox = 32;                          // rows per tensor copy
+constexpr int kWinBytes = 2 * kWinRows * 128;        // K window, then V window
+
+struct alignas(64) WinMaps {
+    CUtensorMap k, v;   // K and V as [rows][64] bf16, boxes of kWinBox rows, 128-byte swizzle
+};
+
+// Rows [row, row + kWinBox) of the tensor `map` describes into shared memory
+// at dst (1024-byte aligned), completion counted in bytes on `bar`; rows
+// past the tensor's end arrive as zeros.
+__device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int row, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The lane's 32-byte run (16-byte chunks 2 sub and 2 sub + 1) of local row
+// kl of a window written with the 128-byte swizzle, under which chunk c of
+// row r sits at byte 16 (c ^ (r & 7)) of the row.  In words, the same order
+// as a 256-bit global load of the run.  The eight lanes of a shared-memory
+// phase (two consecutive rows, four lanes each) meet eight bank groups.
+__device__ __forceinline__ void win_run(const uint8_t *win, int kl, int sub, uint32_t *w) {
+    const int a0 = kl * 128 + ((((2 * sub) ^ kl) & 7) << 4);
+    const uint4 x = *reinterpret_cast<const uint4 *>(win + a0);
+    const uint4 y = *reinterpret_cast<const uint4 *>(win + (a0 ^ 16));
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
+}
+
+// Entries [nb, ne) of the ascending table with |off| <= dmax.  Warp-collective.
+__device__ __forceinline__ void near_range(const int *off, int cnt, int dmax, int &nb, int &ne) {
+    const int lane = threadIdx.x & 31;
+    int below = 0, upto = 0;
+    for (int base = 0; base < cnt; base += 32) {
+        const int t = base + lane;
+        const bool e = t < cnt;
+        const int o = e ? off[t] : 0;
+        below += __popc(__ballot_sync(kFullMask, e && o < -dmax));
+        upto += __popc(__ballot_sync(kFullMask, e && o <= dmax));
+    }
+    nb = below;
+    ne = max(nb, upto);
+}
+
+// Rows [first, first + 8) of head bh (one warp; first < N); the block's
+// window holds key rows [wb, we) of the head for the entries [nb, ne).
+template <bool W16>
+__device__ __forceinline__ void fwd_window_rows(const TableArg &tab, const StreamParams &p, const int *s_off, int cnt,
+                                                int bh, int first, const uint8_t *win, int wb, int we, int nb, int ne,
+                                                uint64_t *bar, volatile int *abort) {
+    using S = Run<__nv_bfloat16, 4>;
+    constexpr int G = 4, R = 8, RB = 128;
+    const int N = tab.N;
+    const int lane = threadIdx.x & 31, sub = lane % G;
+    const int last = min(N, first + R) - 1;
+    const bool valid = first + lane / G < N;
+    const int j = valid ? first + lane / G : last;
+    int tb, te;
+    trim(s_off, cnt, N, first, last, tb, te);
+
+    const size_t row0 = (size_t)bh * N;
+    const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB + sub * S::kBytes;
+    const uint8_t *gV = static_cast<const uint8_t *>(p.V) + row0 * RB + sub * S::kBytes;
+    S q;
+    q.load(static_cast<const uint8_t *>(p.Q) + (row0 + j) * RB + sub * S::kBytes);
+    float2 acc[S::kPairs];
+#pragma unroll
+    for (int i = 0; i < S::kPairs; ++i) acc[i] = make_float2(0.f, 0.f);
+    float m = kMInit, l = 0.f, lt = 0.f;
+    const float sl2 = p.scale_log2;
+    auto raise = [&](float s) {
+        if (s > m + 8.f) {
+            const float a = fast_exp2(m - s);
+            l *= a;
+            lt *= a;
+#pragma unroll
+            for (int i = 0; i < S::kPairs; ++i) acc[i] = mul2(acc[i], make_float2(a, a));
+            m = s;
+        }
+    };
+    auto add = [&](const S &v, float pr) {
+        l += pr;
+        if constexpr (W16) {
+            const uint32_t p2 = bf16x2_splat(pr);
+            lt += __uint_as_float(p2 << 16);
+            v.axpy_p2(p2, acc);
+        } else {
+            v.axpy(pr, acc);
+        }
+    };
+    // far entries [ta, tz) from global memory, two per step
+    auto far = [&](int ta, int tz) {
+        int t = ta;
+        for (; t + 1 < tz; t += 2) {
+            const int k0 = j + s_off[t], k1 = j + s_off[t + 1];
+            const bool in0 = valid && k0 >= 0 && k0 < N, in1 = valid && k1 >= 0 && k1 < N;
+            const size_t c0 = (size_t)min(max(k0, 0), N - 1) * RB, c1 = (size_t)min(max(k1, 0), N - 1) * RB;
+            S ka, kb, va, vb;
+            ka.load(gK + c0);
+            kb.load(gK + c1);
+            va.load(gV + c0);
+            vb.load(gV + c1);
+            float s0 = lanes_sum<G>(q.dot(ka)) * sl2, s1 = lanes_sum<G>(q.dot(kb)) * sl2;
+            s0 = in0 ? s0 : -INFINITY;
+            s1 = in1 ? s1 : -INFINITY;
+            raise(fmaxf(s0, s1));
+            add(va, fast_exp2(s0 - m));
+            add(vb, fast_exp2(s1 - m));
+        }
+        if (t < tz) {
+            const int k0 = j + s_off[t];
+            const bool in0 = valid && k0 >= 0 && k0 < N;
+            const size_t c0 = (size_t)min(max(k0, 0), N - 1) * RB;
+            S ka, va;
+            ka.load(gK + c0);
+            va.load(gV + c0);
+            float s0 = lanes_sum<G>(q.dot(ka)) * sl2;
+            s0 = in0 ? s0 : -INFINITY;
+            raise(s0);
+            add(va, fast_exp2(s0 - m));
+        }
+    };
+    far(tb, min(te, nb));
+    far(max(tb, ne), te);
+    const int na = max(tb, nb), nz = min(te, ne);
+    if (na < nz) {
+        // near entries from the window (its copies were issued before the far loop)
+        mbar_wait(bar, 0, abort);
+        const int jw = j - wb, wl = we - wb - 1;   // key j + off at local row jw + off, clamped into [0, wl]
+        const uint8_t *wV = win + kWinRows * RB;
+        int t = na;
+        for (; t + 1 < nz; t += 2) {
+            const int k0 = j + s_off[t], k1 = j + s_off[t + 1];
+            const bool in0 = valid && k0 >= 0 && k0 < N, in1 = valid && k1 >= 0 && k1 < N;
+            const int l0 = min(max(jw + s_off[t], 0), wl), l1 = min(max(jw + s_off[t + 1], 0), wl);
+            S ka, kb, va, vb;
+            win_run(win, l0, sub, ka.w);
+            win_run(win, l1, sub, kb.w);
+            win_run(wV, l0, sub, va.w);
+            win_run(wV, l1, sub, vb.w);
+            float s0 = lanes_sum<G>(q.dot(ka)) * sl2, s1 = lanes_sum<G>(q.dot(kb)) * sl2;
+            s0 = in0 ? s0 : -INFINITY;
+            s1 = in1 ? s1 : -INFINITY;
+            raise(fmaxf(s0, s1));
+            add(va, fast_exp2(s0 - m));
+            add(vb, fast_exp2(s1 - m));
+        }
+        if (t < nz) {
+            const int k0 = j + s_off[t];
+            const bool in0 = valid && k0 >= 0 && k0 < N;
+            const int l0 = min(max(jw + s_off[t], 0), wl);
+            S ka, va;
+            win_run(win, l0, sub, ka.w);
+            win_run(wV, l0, sub, va.w);
+            float s0 = lanes_sum<G>(q.dot(ka)) * sl2;
+            s0 = in0 ? s0 : -INFINITY;
+            raise(s0);
+            add(va, fast_exp2(s0 - m));
+        }
+    }
+    if (!valid) return;
+    const float ln = W16 ? lt : l;
+    S::store(static_cast<uint8_t *>(p.Out) + (row0 + j) * RB + sub * S::kBytes, acc, ln > 0.f ? __frcp_rn(ln) : 0.f);
+    if (sub == 0) p.LSEout[row0 + j] = l > 0.f ? (m + fast_log2(l)) * kLn2 : -INFINITY;
+}
+
+// Dynamic shared memory: up to 1 KB of alignment, the K and V windows, the
+// head's offsets.
+size_t window_smem_bytes(int max_count) { return 1024 + kWinBytes + sizeof(int) * (size_t)std::max(1, max_count); }
+
+// W warps (8W query rows) per block, MINB blocks per SM.
+template <int W, int MINB, bool W16>
+__global__ void __launch_bounds__(W * 32, MINB)
+fwd_window_kernel(const __grid_constant__ TableArg tab, const StreamParams p, const __grid_constant__ WinMaps wm) {
+    constexpr int R = 8;
+    extern __shared__ uint8_t w_smem[];
+    __shared__ uint64_t bar;
+    __shared__ int s_abort;
+    uint8_t *win = w_smem + ((1024u - (smem_u32(w_smem) & 1023u)) & 1023u);
+    int *s_off = reinterpret_cast<int *>(win + kWinBytes);
+    const int N = tab.N;
+    const int bh = (int)blockIdx.x / p.nblk, yb = (int)blockIdx.x % p.nblk;
+    const int h = bh % tab.H, t0 = tab.start[h], cnt = tab.start[h + 1] - t0;
+    for (int t = threadIdx.x; t < cnt; t += blockDim.x) s_off[t] = tab.off[t0 + t];
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        s_abort = 0;
+    }
+    __syncthreads();
+    const int j0 = yb * W * R, jlast = min(N, j0 + W * R) - 1;
+    int nb, ne;
+    near_range(s_off, cnt, (kWinRows - W * R) / 2, nb, ne);
+    int wb = 0, we = 0;
+    if (nb < ne) {
+        wb = max(0, j0 + s_off[nb]);
+        we = min(N, jlast + s_off[ne - 1] + 1);
+        if (we <= wb) nb = ne;
+    }
+    const int nbox = nb < ne ? (we - wb + kWinBox - 1) / kWinBox : 0;   // nbox * kWinBox <= kWinRows
+    grid_dep_wait();
+    grid_dep_launch();
+    if (threadIdx.x == 0 && nbox > 0) {
+        mbar_expect_tx(&bar, (uint32_t)nbox * kWinBox * 128 * 2);
+        const int y = bh * N + wb;
+        for (int i = 0; i < nbox; ++i) {
+            tma_rows(win + i * kWinBox * 128, &wm.k, y + i * kWinBox, &bar);
+            tma_rows(win + kWinRows * 128 + i * kWinBox * 128, &wm.v, y + i * kWinBox, &bar);
+        }
+    }
+    const int first = j0 + (int)(threadIdx.x >> 5) * R;
+    if (first < N)
+        fwd_window_rows<W16>(tab, p, s_off, cnt, bh, first, win, wb, we, nb, ne, &bar, &s_abort);   // whole warps
+    // the copies land before the block leaves, whatever its warps did
+    if (threadIdx.x == 0 && nbox > 0) mbar_drain(&bar, 0);
 }
 
 // ----------------------------------------------------------------- backward
@@ -628,6 +863,88 @@ cudaError_t fwd_stream(const FwdArgs &a) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled from the driver (through the runtime's entry-point
+// query, so the library needs no link against libcuda); null if unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// A bf16 tensor of `rows` rows of 64 elements (128-byte rows) at `base`,
+// read in boxes of kWinBox rows with the 128-byte swizzle.
+bool window_map(CUtensorMap *m, const void *base, long rows) {
+    const EncodeTiledFn f = encode_tiled();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {64, kWinBox};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The near-window forward, on request (FIBATT_STREAM_WINDOW=1): bf16 rows,
+// no global token, row coordinates within int32.  Measured slower than the
+// plain streaming forward (video 43.2 against 34.3 us, 128 x 128 image 189.9
+// against 149.8 us): 18% more instructions (a 32-byte run takes two 128-bit
+// shared-memory loads where one 256-bit global load did, plus the swizzled
+// addressing), 21 instead of 29 warps per SM (64 KB of shared memory and 80
+// registers per block), for 17% less L2-to-SM traffic.
+bool window_enabled(const FwdArgs &a) {
+    const char *e = getenv("FIBATT_STREAM_WINDOW");
+    if (!(e && atoi(e) == 1)) return false;
+    return a.dtype == FIBATT_BF16 && !a.tab->global0 &&
+           (long)a.B * a.tab->H * a.tab->N + kWinRows < 0x7fffffffL;
+}
+
+// Returns cudaErrorNotSupported (nothing launched) when the tensor maps
+// cannot be made; the caller then takes the plain streaming forward.
+template <int W, int MINB, bool W16>
+cudaError_t fwd_window(const FwdArgs &a) {
+    constexpr int R = 8;
+    const TableArg &tab = *a.tab;
+    const long rows = (long)a.B * tab.H * tab.N;
+    WinMaps wm;
+    if (!window_map(&wm.k, a.K, rows) || !window_map(&wm.v, a.V, rows)) return cudaErrorNotSupported;
+    StreamParams p{};
+    p.Q = a.Q;
+    p.K = a.K;
+    p.V = a.V;
+    p.Out = a.O;
+    p.LSEout = a.LSE;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.nblk = (tab.N + R * W - 1) / (R * W);
+    const size_t smem = window_smem_bytes(tab.max_count);
+    static size_t smem_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto kern = fwd_window_kernel<W, MINB, W16>;
+    if (dev < 0 || dev >= 64 || smem_set[dev] < smem) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) smem_set[dev] = smem;
+    }
+    const long blocks = (long)a.B * tab.H * p.nblk;
+    const cudaError_t e =
+        launch_kernel(kern, dim3((unsigned)blocks), dim3(W * 32), smem, a.stream, pdl_enabled(), tab, p, wm);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <typename T, int G, int W = kStreamWarps, bool GT = false>
 cudaError_t bwd_stream(const BwdArgs &a) {
     constexpr int R = 32 / G;
@@ -686,6 +1003,20 @@ cudaError_t launch_fwd_stream(const FwdArgs &a) {
         return a.dtype == FIBATT_F32 ? fwd_stream<float, 4, false, kStreamWarps, true>(a)
                                      : fwd_stream<__nv_bfloat16, 4, true, kStreamWarps, true>(a);
     if (a.dtype == FIBATT_F32) return fwd_stream<float, 4, false>(a);
+    if (window_enabled(a) && stream_lanes() == 4) {
+        // FIBATT_WINDOW_SHAPE: 0 (8 warps, 3 blocks per SM, 80 registers) or 1 (10 warps, 2 blocks, 84
+        // registers)
+        const char *e = getenv("FIBATT_WINDOW_SHAPE");
+        const int shape = e ? atoi(e) : 0;
+        cudaError_t r;
+        if (!w16)
+            r = fwd_window<8, 3, false>(a);
+        else if (shape == 1)
+            r = fwd_window<10, 2, true>(a);
+        else
+            r = fwd_window<8, 3, true>(a);
+        if (r != cudaErrorNotSupported) return r;
+    }
     if (stream_lanes() == 2)
         return w16 ? fwd_stream<__nv_bfloat16, 2, true>(a) : fwd_stream<__nv_bfloat16, 2, false>(a);
     if (!w16) return fwd_stream<__nv_bfloat16, 4, false>(a);
@@ -699,6 +1030,15 @@ cudaError_t launch_bwd_stream(const BwdArgs &a) {
     if (a.dtype == FIBATT_F32) return bwd_stream<float, 4>(a);
     if (stream_lanes() == 2) return bwd_stream<__nv_bfloat16, 2>(a);
     return stream_warps() == 8 ? bwd_stream<__nv_bfloat16, 4, 8>(a) : bwd_stream<__nv_bfloat16, 4, 4>(a);
+}
+
+// This file's copy of the device error word (each translation unit that
+// includes tma_common.cuh has its own).
+cudaError_t read_stream_device_error(unsigned *code, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned));
+    if (e != cudaSuccess || !clear || *code == 0) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
 }
 
 size_t stream_bwd_scratch_bytes(const TableArg &tab, int B) {

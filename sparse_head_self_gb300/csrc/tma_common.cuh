@@ -18,7 +18,9 @@
 namespace fibatt {
 
 // Device error word (bit flags), read and cleared by fibatt_device_error().
-// Only resident.cu includes this header, so the word has one definition.
+// The library is built without relocatable device code, so each translation
+// unit that includes this header (resident.cu, stream.cu) has its own copy;
+// read_device_error() reads and clears all of them.
 static __device__ unsigned int g_device_error = 0;
 constexpr unsigned kErrWaitTimeout = 1u;
 constexpr unsigned kErrDrainTimeout = 2u;   // a producer left before its last copies landed

@@ -28,11 +28,15 @@ def kernel_path(request, monkeypatch):
     or auto (the library's choice)."""
     path = getattr(request, "param", "auto")
     monkeypatch.delenv("FIBATT_STREAM", raising=False)
+    monkeypatch.delenv("FIBATT_STREAM_WINDOW", raising=False)
     if path == "auto":
         monkeypatch.delenv("FIBATT_PATH", raising=False)
     elif path == "flat_legacy":   # the flat kernels that predate the streaming ones
         monkeypatch.setenv("FIBATT_PATH", "flat")
         monkeypatch.setenv("FIBATT_STREAM", "0")
+    elif path == "flat_window":   # the streaming forward with the near window staged (on request)
+        monkeypatch.setenv("FIBATT_PATH", "flat")
+        monkeypatch.setenv("FIBATT_STREAM_WINDOW", "1")
     else:
         monkeypatch.setenv("FIBATT_PATH", path)
     return path
@@ -85,7 +89,7 @@ def test_video_shape_one_batch_fwd_full():
     _fwd_full(wl, seed=7)
 
 
-@pytest.mark.parametrize("kernel_path", ["generic", "flat", "flat_legacy"], indirect=True)
+@pytest.mark.parametrize("kernel_path", ["generic", "flat", "flat_window", "flat_legacy"], indirect=True)
 def test_video_shape_two_heads_bwd_full(kernel_path):
     # every row of two heads (the narrowest and the widest window) of one
     # batch element: every gradient compared with the oracle's
@@ -113,6 +117,33 @@ def test_edge_sizes(N, diag, kernel_path):
     wl = Workload("edge", 2, H, N, 64, "f32", 1, N, diag, True)
     _fwd_full(wl, seed=N)
     _bwd_full(wl, seed=N)
+
+
+@pytest.mark.parametrize("shape", ["0", "1"])
+@pytest.mark.parametrize("N", [1, 5, 63, 64, 65, 81, 200, 300, 1569])
+def test_window_forward_bf16(N, shape, monkeypatch):
+    # the streaming forward that stages the key and value rows of the near
+    # table entries (|offset| up to 88 or 96) in shared memory (a variant
+    # taken on request; the plain streaming forward is faster): six Wythoff
+    # heads (near entries only, near and far, far only) and three heads of
+    # every distance below 170 (near and far entries side by side; the whole
+    # table stays within the 1024-entry limit), every output against the
+    # oracle; block edges at 64 and 80 rows, windows clipped at both ends of
+    # the sequence
+    monkeypatch.setenv("FIBATT_PATH", "flat")
+    monkeypatch.delenv("FIBATT_STREAM", raising=False)
+    monkeypatch.setenv("FIBATT_STREAM_WINDOW", "1")
+    monkeypatch.setenv("FIBATT_WINDOW_SHAPE", shape)
+    wl = Workload("window", 2, 6, N, 64, "bf16", 1, N, True, True)
+    _fwd_full(wl, seed=N + 11)
+    wl = Workload("window_dense", 2, 3, N, 64, "bf16", 1, N, True, True)
+    q, k, v, _ = make_inputs(wl, N + 12, with_grad=False)
+    dist = list(range(min(N, 170)))
+    sup = api.Support.from_distances(N, [dist] * wl.H, True)
+    O, L = api.fwd(sup, *to_dev(q, k, v), wl.scale)
+    O_ref, L_ref = oracle.fwd(q, k, v, [oracle.Head(dist, N, True)] * wl.H, wl.scale)
+    assert_close("window dense O", O.float().cpu(), O_ref, "bf16")
+    assert_close("window dense LSE", L.cpu(), L_ref, "bf16", lse=True)
 
 
 def _offset_view(t, elems):
