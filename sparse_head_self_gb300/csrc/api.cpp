@@ -376,8 +376,9 @@ fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, c
         e = launch_fwd_generic(a);
     } else if (sel != PathSel::Flat && cached_plan(s, false, s->impl.tab, B, dtype, &pl)) {
         e = launch_fwd_resident(a, pl);
-        // fused: the whole-head units wrote row 0; the last wave's pieces did not
-        if (s->impl.tab.global0 && pl.fuse_row0) row0_from = pl.n_keep;
+        // fused: every head's row 0 was written by its whole-head unit or by
+        // the last-wave piece that holds query 0
+        if (s->impl.tab.global0 && pl.fuse_row0) row0_from = (long)B * s->impl.tab.H;
     } else {
         if (sel == PathSel::Resident)
             return set_error(FIBATT_ERR_UNSUPPORTED, "FIBATT_PATH=resident: windows do not fit in shared memory");

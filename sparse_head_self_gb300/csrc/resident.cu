@@ -230,6 +230,12 @@ __device__ __forceinline__ Unit unit_geometry(const TableArg &tab, const int *st
         g.lo = max(0, g.q0 + off[g.t0]);
         g.nrows = max(0, min(tab.N, g.q1 + off[g.t1 - 1]) - g.lo);
     }
+    // with the dense row 0 fused (whole-head units), the unit or last-wave
+    // piece that holds query 0 stages every key row for it
+    if (p.fuse_row0 && g.q0 == 0 && g.q1 > 0) {
+        g.lo = 0;
+        g.nrows = tab.N;
+    }
     return g;
 }
 
@@ -559,7 +565,7 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
         const Unit g = s_unit[s];
         const uint8_t *st = smem + (size_t)s * p.stage_bytes;
         if constexpr (GT) {
-            if (p.fuse_row0 && g.q0 == 0 && g.q1 == tab.N && g.lo == 0 && g.nrows == tab.N) {
+            if (p.fuse_row0 && g.q0 == 0 && g.q1 > 0 && g.lo == 0 && g.nrows == tab.N) {
                 // stage s's partial slot, after the stages: gwarps x 32
                 // float2 partial accumulators, then gwarps maxima and sums
                 const size_t row0 = (size_t)g.bh * tab.N;
@@ -1641,21 +1647,16 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->grid = (int)std::min<long>(units, sms);
     const long left = units > pl->grid ? units % pl->grid : 0;   // units of the last, partial wave
     // With the global first token and whole-head units, row 0 of every head
-    // is computed inside its unit (fused_row0).  That needs every head's
-    // table non-empty (so that its unit stages all N key rows) and room for a
-    // partial-state slot per stage; and it keeps the last wave's units whole,
-    // so it is taken when that wave is empty or at least a quarter full (a
-    // few whole units in a last wave cost more than the separate row kernel
-    // with last-wave pieces), or when there are many waves, the row kernel's
-    // cost growing with the heads (B = 256, ViT-B shape, 20.2 waves: fused
-    // 112.0 us against 123.6 us; B = 64, 5.05 waves: 33.6 against 32.5 us).
+    // is computed inside its unit (fused_row0), or, for the last wave's
+    // pieces, inside the piece that holds query 0 (which then stages every
+    // key row of its head).  That needs every head's table non-empty (so that
+    // a whole unit stages all N key rows) and room for a partial-state slot
+    // per stage.
     bool staged_all = true;
     for (int h = 0; h < tab.H; ++h) staged_all = staged_all && tab.start[h + 1] > tab.start[h];
-    pl->fuse_row0 = tab.global0 && qsplit == 1 && staged_all;
-    if (const char *e = getenv("FIBATT_GT_FUSE"))   // 0: never, else whenever possible
+    pl->fuse_row0 = tab.global0 && qsplit == 1 && staged_all && kv_cap >= N;
+    if (const char *e = getenv("FIBATT_GT_FUSE"))   // 0: never (the dense row kernel runs after)
         pl->fuse_row0 = pl->fuse_row0 && atoi(e) != 0;
-    else
-        pl->fuse_row0 = pl->fuse_row0 && (left == 0 || 4 * left >= pl->grid || units >= 8L * pl->grid);
     const size_t slot_bytes = (size_t)gwarps * 33 * sizeof(float2);   // one partial slot per stage
     if (pl->fuse_row0)
         while (stages > 2 && (stage + slot_bytes) * stages > budget) pl->stages = --stages;
@@ -1667,7 +1668,7 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->qsub = 1;
     pl->sub_rows = chunk;
     const char *st = getenv("FIBATT_SPLIT_TAIL");
-    if (left > 0 && !(st && atoi(st) == 0) && !pl->fuse_row0) {
+    if (left > 0 && !(st && atoi(st) == 0)) {
         const int qsub = (int)std::max<long>(1, std::min<long>(chunk / R, pl->grid / left));
         if (qsub > 1) {
             pl->n_keep = (int)(units - left);

@@ -416,15 +416,26 @@ def test_global_token_edge_sizes(N, kernel_path):
                                           ("vitb", "bf16", 38)])
 def test_global_token_whole_heads(name, dtype, B, fuse, monkeypatch):
     # B H >= the SM count: whole-head units, where row 0 is computed inside
-    # the resident forward (fuse 1; by default when the last wave is empty or
-    # at least a quarter full, as for B = 38) or by the dense row kernel
-    # (fuse 0; by default for B = 13, whose last wave has 4 units)
+    # the resident forward (fuse 1, the default) or by the dense row kernel
+    # (fuse 0).  B = 13 leaves 4 units for the last wave, cut into pieces:
+    # the piece holding query 0 stages its whole head and computes row 0;
+    # B = 38 fills whole waves
     monkeypatch.delenv("FIBATT_PATH", raising=False)
     if fuse is None:
         monkeypatch.delenv("FIBATT_GT_FUSE", raising=False)
     else:
         monkeypatch.setenv("FIBATT_GT_FUSE", fuse)
     _global_fwd_bwd(Workload(**{**WORKLOADS[name].__dict__, "B": B, "dtype": dtype}), 25)
+
+
+@pytest.mark.parametrize("fuse", ["1", "0"])
+def test_global_token_vitb_batch_64(fuse, monkeypatch):
+    # the bench's ViT-B shape (768 heads: five waves and a last wave of 8
+    # units, cut into pieces), heads 0, 5 and 11 of every batch element
+    monkeypatch.delenv("FIBATT_PATH", raising=False)
+    monkeypatch.setenv("FIBATT_GT_FUSE", fuse)
+    wl = Workload(**{**WORKLOADS["vitb"].__dict__, "B": 64})
+    _global_fwd_bwd(wl, 27, heads_subset=(0, 5, wl.H - 1))
 
 
 def test_global_token_many_waves():
