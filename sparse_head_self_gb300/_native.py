@@ -11,7 +11,7 @@ import os
 import re
 import threading
 
-from .build import LIB, ROOT
+from .build import LIB, LIB_CHECKS, ROOT
 
 HEADER = os.path.join(ROOT, "include", "fibatt.h")
 
@@ -75,10 +75,11 @@ def lib():
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"libfibatt is not built ({LIB} missing); run "
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libfibatt is not built ({path} missing); run "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
-        L = ctypes.CDLL(LIB)
+        L = ctypes.CDLL(path)
         for name, (res, args) in _SIGS.items():
             fn = getattr(L, name)
             fn.restype = res
@@ -93,4 +94,6 @@ def check(status: int) -> None:
 
 
 def lib_path() -> str:
-    return LIB
+    """The library this process loads: the checks build (bounds-checked
+    kernels) when FIBATT_CHECKS=1 is set, else the regular one."""
+    return LIB_CHECKS if os.environ.get("FIBATT_CHECKS") == "1" else LIB

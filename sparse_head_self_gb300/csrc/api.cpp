@@ -358,6 +358,7 @@ void fibatt_support_destroy(fibatt_support_t s) {
 
 fibatt_status fibatt_fwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
                          const void *V, float scale, void *O, float *LSE, cudaStream_t stream) {
+    const ProfileReport report("fibatt_fwd");
     fibatt_status st = check_common(s, B, D, dtype, scale);
     if (st != FIBATT_OK) return st;
     if ((st = check_tensor(Q, "Q")) || (st = check_tensor(K, "K")) || (st = check_tensor(V, "V")) ||
@@ -428,6 +429,7 @@ static size_t bwd_workspace_needed(fibatt_support_t s, int B, fibatt_dtype dt, B
 fibatt_status fibatt_bwd(fibatt_support_t s, int B, int D, fibatt_dtype dtype, const void *Q, const void *K,
                          const void *V, const void *O, const float *LSE, const void *dO, float scale, void *dQ,
                          void *dK, void *dV, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    const ProfileReport report("fibatt_bwd");
     fibatt_status st = check_common(s, B, D, dtype, scale);
     if (st != FIBATT_OK) return st;
     if ((st = check_tensor(Q, "Q")) || (st = check_tensor(K, "K")) || (st = check_tensor(V, "V")) ||

@@ -3,10 +3,65 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdio>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace fibatt {
+
+// Device error word (bit flags), read and cleared by fibatt_device_error().
+// The library is built without relocatable device code, so every .cu file
+// has its own copy of the word; each defines a reader with
+// FIBATT_DEFINE_ERROR_READER, and read_device_error() (resident.cu) combines
+// them.
+static __device__ unsigned int g_device_error = 0;
+constexpr unsigned kErrWaitTimeout = 1u;    // a bounded mbarrier wait gave up
+constexpr unsigned kErrDrainTimeout = 2u;   // a producer left before its last copies landed
+constexpr unsigned kErrBounds = 4u;         // a bounds check of a FIBATT_CHECKS build failed
+
+// Bounds checks of the debug build (-DFIBATT_CHECKS): FIBATT_CHECKED(cond)
+// is `cond`, and a false one records kErrBounds and the first failing source
+// line (this file's copy of g_check_line); the caller then skips the
+// access.  In the regular build FIBATT_CHECKED(cond) is `true` and costs
+// nothing.
+#ifdef FIBATT_CHECKS
+static __device__ unsigned int g_check_line = 0;
+__device__ __forceinline__ bool check_ok(bool ok, unsigned line) {
+    if (!ok) {
+        atomicOr(&g_device_error, kErrBounds);
+        atomicCAS(&g_check_line, 0u, line);
+    }
+    return ok;
+}
+#define FIBATT_CHECKED(cond) (::fibatt::check_ok((cond), __LINE__))
+#define FIBATT_CHECK_READ_LINE(file)                                                                  \
+    {                                                                                                  \
+        unsigned line = 0;                                                                             \
+        if (cudaMemcpyFromSymbol(&line, g_check_line, sizeof(unsigned)) == cudaSuccess && line) {      \
+            fprintf(stderr, "libfibatt checks: a bounds check failed in %s, line %u\n", file, line); \
+            if (clear) {                                                                               \
+                const unsigned z = 0;                                                                  \
+                cudaMemcpyToSymbol(g_check_line, &z, sizeof(unsigned));                                \
+            }                                                                                          \
+        }                                                                                              \
+    }
+#else
+#define FIBATT_CHECKED(cond) true
+#define FIBATT_CHECK_READ_LINE(file)
+#endif
+
+// Defines `cudaError_t fn(unsigned *code, bool clear)`, the reader of this
+// file's error word (and, in a checks build, the line of its first failed
+// check, printed to stderr).
+#define FIBATT_DEFINE_ERROR_READER(fn, file)                                         \
+    cudaError_t fn(unsigned *code, bool clear) {                                     \
+        cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned)); \
+        if (e != cudaSuccess) return e;                                              \
+        FIBATT_CHECK_READ_LINE(file)                                                 \
+        if (!clear || *code == 0) return cudaSuccess;                                \
+        const unsigned zero = 0;                                                     \
+        return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));          \
+    }
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)

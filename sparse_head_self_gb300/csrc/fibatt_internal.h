@@ -114,11 +114,35 @@ bool cached_plan(const void *support, bool backward, const TableArg &tab, int B,
                  ResidentPlan *pl);
 void forget_plans(const void *support);
 
+// ---- per-kernel timing (FIBATT_PROFILE=1; profile.cpp) ----------------------
+// A ProfileLaunch around each launch records CUDA events on its stream while
+// profiling is on; the ProfileReport of the public call prints the kernels'
+// times to stderr when the call returns.
+class ProfileLaunch {
+  public:
+    ProfileLaunch(cudaStream_t stream, const void *func);
+    ~ProfileLaunch();
+
+  private:
+    cudaStream_t stream_;
+    int slot_ = -1;
+};
+
+class ProfileReport {
+  public:
+    explicit ProfileReport(const char *call) : call_(call) {}
+    ~ProfileReport();
+
+  private:
+    const char *call_;
+};
+
 // Launch `kern` on `stream`; with pdl set, as a programmatic dependent launch
 // (the kernel calls grid_dep_wait before touching global memory).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
                           Args &&...args) {
+    const ProfileLaunch prof(stream, reinterpret_cast<const void *>(kern));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -154,7 +178,11 @@ size_t stream_bwd_scratch_bytes(const TableArg &tab, int B);
 bool stream_row0_in_grid(const TableArg &tab);   // global token: the streaming forward computes the rows 0
 cudaError_t launch_bwd_resident(const BwdArgs &a, const ResidentPlan &pl);
 cudaError_t read_device_error(unsigned *code, bool clear);
-cudaError_t read_stream_device_error(unsigned *code, bool clear);   // stream.cu's copy of the word
+// Each kernel file's own copy of the device error word (device_common.cuh).
+cudaError_t read_error_resident(unsigned *code, bool clear);
+cudaError_t read_error_stream(unsigned *code, bool clear);
+cudaError_t read_error_generic(unsigned *code, bool clear);
+cudaError_t read_error_global_token(unsigned *code, bool clear);
 
 // Global first token (global_token.cu): the dense row of token 0 (forward,
 // after the banded kernel), its dense row before the banded backward, and

@@ -269,4 +269,6 @@ cudaError_t launch_bwd_generic(const BwdArgs &a) {
     return a.dtype == FIBATT_F32 ? bwd_generic<float>(a) : bwd_generic<__nv_bfloat16>(a);
 }
 
+FIBATT_DEFINE_ERROR_READER(read_error_generic, "generic.cu")
+
 }  // namespace fibatt

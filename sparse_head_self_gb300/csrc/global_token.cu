@@ -200,6 +200,7 @@ int gt_cluster(long heads) {
 template <typename... KArgs, typename... Args>
 cudaError_t launch_cluster(void (*kern)(KArgs...), unsigned heads, int c, unsigned threads, cudaStream_t stream,
                            Args &&...args) {
+    const ProfileLaunch prof(stream, reinterpret_cast<const void *>(kern));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(heads * (unsigned)c);
     cfg.blockDim = dim3(threads);
@@ -290,5 +291,7 @@ cudaError_t launch_bwd_global_row(const BwdArgs &a) {
 cudaError_t launch_bwd_global_col(const BwdArgs &a) {
     return a.dtype == FIBATT_F32 ? bwd_global_any<float>(a, false) : bwd_global_any<__nv_bfloat16>(a, false);
 }
+
+FIBATT_DEFINE_ERROR_READER(read_error_global_token, "global_token.cu")
 
 }  // namespace fibatt

@@ -60,6 +60,7 @@ extern "C" fibatt_status fibatt_bwd_noalloc(fibatt_support_t s, int B, int D, fi
                                             const void *K, const void *V, const void *O, const float *LSE,
                                             const void *dO, float scale, void *dQ, void *dK, void *dV,
                                             cudaStream_t stream) {
+    const ProfileReport report("fibatt_bwd_noalloc");
     fibatt_status st = check_bwd_args(s, B, D, dtype, Q, K, V, O, LSE, dO, scale, dQ, dK, dV);
     if (st != FIBATT_OK) return st;
     const TableArg &tab = support_table(s);

@@ -516,7 +516,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1, &s_abort)) break;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)g.bh * tab.N;
-            const uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
+            uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
+            if (!FIBATT_CHECKED(g.q1 - g.q0 <= p.chunk && g.nrows <= p.kv_cap)) qb = kvb = 0;   // the stage's room
             // the consumers read the geometry after the full phase, which
             // this arrive (a release) belongs to
             s_unit[s] = g;
@@ -1103,12 +1104,15 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             const bool fill_by_consumers = i == 0;
             const size_t row0 = (size_t)bwd_item_unit(p, it) * N;
             if (lane == 0) {
-                const uint32_t b = (uint32_t)tens;
+                // the stage holds Q, K, V, dO and the rows' D_j, LSE_j
+                const uint32_t b = FIBATT_CHECKED(4 * tens + 8 * (size_t)N <= p.stage_bytes) ? (uint32_t)tens : 0u;
                 mbar_expect_tx(&full_bar[s], 4 * b);
-                bulk_g2s(st, static_cast<const T *>(p.Q) + row0 * kHeadDim, b, &full_bar[s]);
-                bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
-                bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
-                bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
+                if (b) {
+                    bulk_g2s(st, static_cast<const T *>(p.Q) + row0 * kHeadDim, b, &full_bar[s]);
+                    bulk_g2s(st + tens, static_cast<const T *>(p.K) + row0 * kHeadDim, b, &full_bar[s]);
+                    bulk_g2s(st + 2 * tens, static_cast<const T *>(p.V) + row0 * kHeadDim, b, &full_bar[s]);
+                    bulk_g2s(st + 3 * tens, static_cast<const T *>(p.dO) + row0 * kHeadDim, b, &full_bar[s]);
+                }
                 if (fill_by_consumers) {   // the consumers compute these D_j
                     bulk_prefetch_l2(static_cast<const T *>(p.O) + row0 * kHeadDim, b);
                     if ((N * 4) % 16 == 0 && (row0 * 4) % 16 == 0) bulk_prefetch_l2(p.LSE + row0, (uint32_t)N * 4);
@@ -1184,7 +1188,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         const int u = bwd_item_unit(p, it);
         const bool piece = !GT && it >= p.n_keep;   // the plan splits no unit with the global token
         const int h = u % tab.H;
-        const int t0 = s_start[h], t1 = s_start[h + 1];
+        const int t0 = s_start[h];
+        // the (P, dS) scratch and the pieces' areas hold max_count entries per row
+        const int t1 = FIBATT_CHECKED(s_start[h + 1] - t0 <= p.max_count) ? s_start[h + 1] : t0;
         const size_t row0 = (size_t)u * N;
         if (i == 0) {
             // D_j = <dO_j, O_j> and LSE_j (log2 units), one row per consumer
@@ -1936,14 +1942,20 @@ cudaError_t launch_fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
 }
 
 // Read (and optionally clear) the device error word of the current device.
+FIBATT_DEFINE_ERROR_READER(read_error_resident, "resident.cu")
+
+// The device error words of every kernel file, OR-ed (and cleared).
 cudaError_t read_device_error(unsigned *code, bool clear) {
-    unsigned mine = 0, other = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&mine, g_device_error, sizeof(unsigned));
-    if (e == cudaSuccess) e = read_stream_device_error(&other, clear);   // the streaming kernels' word
-    *code = mine | other;
-    if (e != cudaSuccess || !clear || mine == 0) return e;
-    const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+    cudaError_t (*const readers[])(unsigned *, bool) = {read_error_resident, read_error_stream, read_error_generic,
+                                                        read_error_global_token};
+    *code = 0;
+    for (auto r : readers) {
+        unsigned c = 0;
+        const cudaError_t e = r(&c, clear);
+        if (e != cudaSuccess) return e;
+        *code |= c;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace fibatt

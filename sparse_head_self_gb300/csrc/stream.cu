@@ -290,7 +290,7 @@ constexpr int kWinRows = 256;                        // staged key (and value) r
 constexpr int kWinBox = 32;                          // rows per tensor copy
 constexpr int kWinBytes = 2 * kWinRows * 128;        // K window, then V window
 
-struct alignas(64) WinMaps {
+struct WinMaps {
     CUtensorMap k, v;   // K and V as [rows][64] bf16, boxes of kWinBox rows, 128-byte swizzle
 };
 
@@ -311,6 +311,7 @@ __device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int 
 // as a 256-bit global load of the run.  The eight lanes of a shared-memory
 // phase (two consecutive rows, four lanes each) meet eight bank groups.
 __device__ __forceinline__ void win_run(const uint8_t *win, int kl, int sub, uint32_t *w) {
+    if (!FIBATT_CHECKED((unsigned)kl < (unsigned)kWinRows)) kl = 0;
     const int a0 = kl * 128 + ((((2 * sub) ^ kl) & 7) << 4);
     const uint4 x = *reinterpret_cast<const uint4 *>(win + a0);
     const uint4 y = *reinterpret_cast<const uint4 *>(win + (a0 ^ 16));
@@ -487,7 +488,8 @@ fwd_window_kernel(const __grid_constant__ TableArg tab, const StreamParams p, co
         we = min(N, jlast + s_off[ne - 1] + 1);
         if (we <= wb) nb = ne;
     }
-    const int nbox = nb < ne ? (we - wb + kWinBox - 1) / kWinBox : 0;   // nbox * kWinBox <= kWinRows
+    int nbox = nb < ne ? (we - wb + kWinBox - 1) / kWinBox : 0;   // nbox * kWinBox <= kWinRows
+    if (!FIBATT_CHECKED(nbox * kWinBox <= kWinRows)) nbox = 0, nb = ne;
     grid_dep_wait();
     grid_dep_launch();
     if (threadIdx.x == 0 && nbox > 0) {
@@ -660,7 +662,8 @@ __device__ __forceinline__ void key_rows(const TableArg &tab, const StreamParams
         // dQ errors within a few thousandths of the bf16 bound
         gg.axpy(P, dv);
         qq.axpy(dS, dk);
-        if (in && sub == 0) scr[(ptrdiff_t)j - (ptrdiff_t)t * p.ns] = dS;
+        if (in && sub == 0 && FIBATT_CHECKED(t < cnt && cnt <= p.max_count && j < p.ns))
+            scr[(ptrdiff_t)j - (ptrdiff_t)t * p.ns] = dS;
     }
     if constexpr (GT) {
         // global first token: the pair (0, k) for every key k >= 1 whose band
@@ -759,6 +762,7 @@ bwd_query_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams
     const size_t lo = sub * S::kBytes;
     const uint8_t *gK = static_cast<const uint8_t *>(p.K) + row0 * RB + lo;
     const float *scr = p.scr + (size_t)bh * p.max_count * p.ns + j;
+    if (!FIBATT_CHECKED(te <= cnt && cnt <= p.max_count && j < p.ns)) te = tb;   // the scratch's rows
     float2 dq[S::kPairs];
 #pragma unroll
     for (int i = 0; i < S::kPairs; ++i) dq[i] = make_float2(0.f, 0.f);
@@ -1032,14 +1036,7 @@ cudaError_t launch_bwd_stream(const BwdArgs &a) {
     return stream_warps() == 8 ? bwd_stream<__nv_bfloat16, 4, 8>(a) : bwd_stream<__nv_bfloat16, 4, 4>(a);
 }
 
-// This file's copy of the device error word (each translation unit that
-// includes tma_common.cuh has its own).
-cudaError_t read_stream_device_error(unsigned *code, bool clear) {
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned));
-    if (e != cudaSuccess || !clear || *code == 0) return e;
-    const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
-}
+FIBATT_DEFINE_ERROR_READER(read_error_stream, "stream.cu")
 
 size_t stream_bwd_scratch_bytes(const TableArg &tab, int B) {
     const size_t rows = (size_t)B * tab.H * tab.N, heads = (size_t)B * tab.H;

@@ -17,13 +17,6 @@
 
 namespace fibatt {
 
-// Device error word (bit flags), read and cleared by fibatt_device_error().
-// The library is built without relocatable device code, so each translation
-// unit that includes this header (resident.cu, stream.cu) has its own copy;
-// read_device_error() reads and clears all of them.
-static __device__ unsigned int g_device_error = 0;
-constexpr unsigned kErrWaitTimeout = 1u;
-constexpr unsigned kErrDrainTimeout = 2u;   // a producer left before its last copies landed
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -13,20 +13,23 @@ import pytest
 
 import oracle
 from sparse_head_self_gb300 import _native, api
-from sparse_head_self_gb300.build import build_library
+from sparse_head_self_gb300.build import build_all
 from sparse_head_self_gb300.inputs import WORKLOADS
 
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
-    build_library()
+    build_all()
     yield
 
 
-def test_exports_every_header_function():
+@pytest.mark.parametrize("checks", [False, True])
+def test_exports_every_header_function(checks):
+    # the library and its bounds-checked debug build (both made by build())
+    from sparse_head_self_gb300.build import LIB, LIB_CHECKS
     names = _native.header_functions()
     assert "fibatt_fwd" in names and "fibatt_bwd" in names and "fibatt_support_build" in names
-    L = ctypes.CDLL(_native.lib_path())
+    L = ctypes.CDLL(LIB_CHECKS if checks else LIB)
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
     assert set(names) == set(_native._SIGS), "ctypes signatures out of sync with the header"
