@@ -556,6 +556,8 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     if (grp >= p.groups) return;
     const LaneGeom<T, G> lg;
     const int rpu = p.chunk / R;
+    const int rot_step = rpu % p.gwarps;
+    int rot = 0;
     for (int i = grp;; i += p.groups) {
         const int u = fwd_slot_unit(p, i);
         if (u < 0) break;
@@ -578,7 +580,13 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
                               static_cast<T *>(p.O) + row0 * kHeadDim, p.LSE + row0);
             }
         }
-        for (int r = wg; r < rpu; r += p.gwarps)
+        // round r of the group's k-th unit goes to warp (r + k rpu) mod gwarps:
+        // with fewer warps than rounds the extra rounds circulate over the
+        // warps from unit to unit (rot = k rpu mod gwarps, kept incrementally)
+        const int r0 = wg >= rot ? wg - rot : wg - rot + p.gwarps;
+        rot += rot_step;
+        if (rot >= p.gwarps) rot -= p.gwarps;
+        for (int r = r0; r < rpu; r += p.gwarps)
             fwd_round<T, G, UNROLL, GT, true>(tab, s_off, p, g, st + q_off, st + k_off, (ptrdiff_t)(v_off - k_off), r, lg,
                                     st + g0_off, st + g0_off + RB);
         __syncwarp();
@@ -1634,7 +1642,8 @@ bool plan_fwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     const int rounds = chunk / R;
     int groups = stages >= 2 && 2 * rounds <= maxw - 1 ? 2 : 1;
     if (const char *e = getenv("FIBATT_GROUPS")) groups = std::max(1, std::min(2, atoi(e)));
-    const int gwarps = std::max(1, std::min(rounds, (maxw - 1) / groups));
+    int gwarps = std::max(1, std::min(rounds, (maxw - 1) / groups));
+    if (const char *e = getenv("FIBATT_FWD_GWARPS")) gwarps = std::max(1, std::min(gwarps, atoi(e)));
     int prefetch = 0;   // L2 warming of later units measured slower: off by default
     if (const char *e = getenv("FIBATT_PREFETCH")) prefetch = std::max(0, std::min(8, atoi(e)));
     pl->prefetch = prefetch;
