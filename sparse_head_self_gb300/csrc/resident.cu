@@ -931,6 +931,35 @@ __device__ __forceinline__ void bwd_b_global(const int *off, int t0, int t1, int
     gg.axpy(P, dv);
 }
 
+// Global first token in a last-wave piece, phase B: the pair (0, k) for a
+// key row k >= 1 whose band misses query 0, with P_0k and dS_0k computed
+// here from the staged rows (query and dO row 0 at sQ and sQ + gdelta; key
+// and value row k at sK + k RB and sK + vdelta + k RB; D_0, LSE_0 in log2
+// units); acc += dS_0k q_0 (dk, which = 0) or P_0k dO_0 (dv, which = 1).
+template <typename T, int G>
+__device__ __forceinline__ void bwd_b_global_local(const int *off, int t0, int t1, int k, bool valid,
+                                                   const uint8_t *sQ, ptrdiff_t gdelta, const uint8_t *sK,
+                                                   ptrdiff_t vdelta, float D0, float L0, float sl2,
+                                                   const LaneGeom<T, G> &lg, int which, float2 (&acc)[32 / G]) {
+    constexpr int RB = Slice<T, G>::kRowBytes;
+    // every lane takes part in the warp-wide scan, whatever its row
+    const int first = __shfl_sync(kFullMask, k, 0);   // the warp's rows are first + lane / G
+    const unsigned hit = band_reaches_zero(off, t0, t1, first, 32 / G);
+    const bool need = valid && k >= 1 && !((hit >> (k - first)) & 1u);
+    Slice<T, G> q0, g0, kk, vv;
+    q0.load(sQ, lg.c);
+    g0.load(sQ + gdelta, lg.c);
+    kk.load(sK + (ptrdiff_t)k * RB, lg.c);
+    vv.load(sK + vdelta + (ptrdiff_t)k * RB, lg.c);
+    const float sc = group_sum<G>(q0.dot(kk));
+    const float dp = group_sum<G>(g0.dot(vv));
+    const float P = need ? fast_exp2(fmaf(sc, sl2, -L0)) : 0.f;
+    if (which == 0)
+        q0.axpy(P * (dp - D0), acc);
+    else
+        g0.axpy(P, acc);
+}
+
 // Half of the dot product of two 64-element rows in shared memory: the
 // lane's half (lane & 1) of the dims, in 16-byte chunks whose order is
 // rotated by rot and the half, so that the eight lanes of a quarter warp (four
@@ -1194,7 +1223,9 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
         const uint8_t *sQ = st, *sK = st + tens;
         const float *sD = reinterpret_cast<const float *>(st + 4 * tens), *sL = sD + N;
         const int u = bwd_item_unit(p, it);
-        const bool piece = !GT && it >= p.n_keep;   // the plan splits no unit with the global token
+        // with the global token the plan cuts units into one-round pieces only
+        // (the piece_par path below), with the dense parts fused
+        const bool piece = it >= p.n_keep;
         const int h = u % tab.H;
         const int t0 = s_start[h];
         // the (P, dS) scratch and the pieces' areas hold max_count entries per row
@@ -1219,7 +1250,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             // compute the key round's (P, dS) for a share of the offsets each,
             // then one warp accumulates dK and one dV over all of them.  A
             // piece is always its CTA's last item (the plan keeps the pieces
-            // within one wave).
+            // within one wave).  With the global token, the pairs (j, 0) and
+            // (0, k) of the round's rows are added by the warps that store
+            // them, and the piece of round 0 has its spare warps compute the
+            // dense row 0 and column 0 over the staged head.
             const int r = (it - p.n_keep) % p.pieces;
             const int lr = lane / G;
             int tb = t0, te = t0;
@@ -1247,7 +1281,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                 if (cw == 0) {
                     for (int a = 0; a < kPieceA - 1; ++a)
                         acc_add_from_shared<T, G>(pa + ((size_t)a * R + lr) * kHeadDim, lg.c, dq);
-                    if (valid) {
+                    if constexpr (GT)
+                        bwd_a_global<T, G>(s_off, t0, t1, j, valid, sK, (ptrdiff_t)tens, qr, g, sD[j], sL[j],
+                                           p.scale_log2, lg, dq);
+                    if (valid && !(GT && j == 0)) {   // dQ_0: the dense row (spare warps of round 0's piece)
 #pragma unroll
                         for (int x = 0; x < 32 / G; ++x) dq[x] = mul2(dq[x], make_float2(p.scale, p.scale));
                         S::store(static_cast<T *>(p.dQ) + (row0 + j) * kHeadDim, lg.c, dq);
@@ -1283,7 +1320,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                         rr.load(src + (size_t)jc * RB, lg.c);
                         rr.axpy(b == 0 ? w.y : w.x, acc);
                     }
-                    if (valid) {
+                    if constexpr (GT)
+                        bwd_b_global_local<T, G>(s_off, t0, t1, k, valid, sQ, (ptrdiff_t)(3 * tens), sK,
+                                                 (ptrdiff_t)tens, sD[0], sL[0], p.scale_log2, lg, b, acc);
+                    if (valid && !(GT && k == 0)) {   // dK_0, dV_0: the dense column (round 0's piece)
                         if (b == 0) {
 #pragma unroll
                             for (int x = 0; x < 32 / G; ++x) acc[x] = mul2(acc[x], make_float2(p.scale, p.scale));
@@ -1291,6 +1331,19 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
                         S::store(static_cast<T *>(b == 0 ? p.dK : p.dV) + (row0 + k) * kHeadDim, lg.c, acc);
                     }
                 }
+            } else if (GT && r == 0) {
+                // spare warps of round 0's piece: the weights of row 0 and
+                // column 0 over the staged head, then the three dense sums
+                // (gt_fused_weights / gt_fused_sums, as in a whole unit)
+                const int sw = cw - (kPieceA + kPieceB), nsw = p.cwarps - (kPieceA + kPieceB);
+                float *w0r = reinterpret_cast<float *>(smem + p.gt_off), *w0c = w0r + 2 * N;
+                gt_fused_weights<T>(sQ, tens, sD, sL, N, sw, nsw, p.scale_log2, w0r, w0c);
+                named_sync(4, 32 * nsw);
+                float2 *part = reinterpret_cast<float2 *>(w0c + 2 * N);
+                for (int item = sw; item < 3 * kGtParts; item += nsw)
+                    gt_fused_sums<T>(sQ, tens, N, item, w0r, w0c, part, &s_gt_count, p.scale,
+                                     static_cast<T *>(p.dQ) + row0 * kHeadDim, static_cast<T *>(p.dK) + row0 * kHeadDim,
+                                     static_cast<T *>(p.dV) + row0 * kHeadDim);
             }
             consumer_sync(cthreads);   // stage free
             if (cw == 0 && lane == 0) mbar_arrive(&empty_bar[s]);
@@ -1775,7 +1828,7 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
     pl->n_keep = units;
     pl->qsub = 1;       // pieces per unit
     pl->sub_rows = rounds;   // rounds per piece
-    bool pieces = left > 0 && units > pl->grid && !tab.global0;
+    bool pieces = left > 0 && units > pl->grid;
     if (const char *e = getenv("FIBATT_BWD_PIECES")) pieces = pieces && atoi(e) != 0;
     pl->split_off = 0;
     pl->piece_par = 0;
@@ -1783,21 +1836,26 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
         int optin = 0;
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         const size_t static_smem = 2048 + sizeof(int) * kMaxEntries;   // barriers + offsets, rounded up
+        const size_t pa_bytes = (size_t)kPieceA * R * kHeadDim * sizeof(float);
+        const size_t pw_bytes = (size_t)R * std::max(1, tab.max_count) * 8;   // one round's (P, dS)
         for (int pr = 1; pr <= 2; ++pr) {
             const int np = (rounds + pr - 1) / pr;
-            const size_t area = (size_t)pr * R * std::max(1, tab.max_count) * 8;   // (P, dS) per phase-B warp
+            // one-round pieces over kPieceA + kPieceB warps: the partial dQ
+            // rows and the round's (P, dS) go to the unit scratch, which
+            // pieces use for nothing else
+            bool par = pr == 1 && pl->gwarps >= kPieceA + kPieceB && scratch >= pa_bytes + pw_bytes;
+            if (const char *e = getenv("FIBATT_BWD_PIECE_PAR")) par = par && atoi(e) != 0;
+            // global token: one-round pieces only, with spare warps for the dense parts
+            if (tab.global0 && !(par && pl->gwarps > kPieceA + kPieceB)) continue;
+            const size_t area = par ? 0 : (size_t)pr * R * std::max(1, tab.max_count) * 8;   // per phase-B warp
             if ((long)left * np <= pl->grid && 2 * pr <= pl->gwarps &&
                 pl->smem + area + static_smem <= (size_t)optin) {
                 pl->n_keep = units - left;
                 pl->qsub = np;
                 pl->sub_rows = pr;
-                pl->split_off = pl->smem;
+                pl->split_off = par ? stage * stages + pa_bytes : pl->smem;
                 pl->smem += area;
-                // one-round pieces over kPieceA + kPieceB warps: the partial
-                // dQ rows go to the P/dS scratch, which must hold them
-                pl->piece_par = pr == 1 && pl->gwarps >= kPieceA + kPieceB &&
-                                scratch >= (size_t)kPieceA * R * kHeadDim * sizeof(float);
-                if (const char *e = getenv("FIBATT_BWD_PIECE_PAR")) pl->piece_par = pl->piece_par && atoi(e) != 0;
+                pl->piece_par = par;
                 break;
             }
         }
@@ -1818,6 +1876,12 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
             pl->fuse_row0 = 1;
             pl->gt_off = pl->smem;
             pl->smem += gt_bytes;
+        } else if (pl->qsub > 1) {   // the pieces compute the dense parts only when fused: whole units
+            pl->n_keep = units;
+            pl->qsub = 1;
+            pl->sub_rows = rounds;
+            pl->split_off = 0;
+            pl->piece_par = 0;
         }
     }
     pl->threads = 32 * (1 + pl->gwarps);
