@@ -171,7 +171,7 @@ std::string tuning_env() {
     std::string r;
     for (const char *n : {"FIBATT_QSPLIT", "FIBATT_LANES", "FIBATT_GROUPS", "FIBATT_STAGES", "FIBATT_BWD_THREADS",
                           "FIBATT_UNROLL", "FIBATT_FWD_THREADS", "FIBATT_PREFETCH", "FIBATT_BWD_LANES", "FIBATT_SPLIT_TAIL",
-                          "FIBATT_BWD_PIECES", "FIBATT_BWD_PIECE_PAR", "FIBATT_GT_FUSE", "FIBATT_FWD_GWARPS"}) {
+                          "FIBATT_BWD_PIECES", "FIBATT_BWD_PIECE_PAR", "FIBATT_GT_FUSE", "FIBATT_FWD_GWARPS", "FIBATT_BWD_PIECE_ROUNDS"}) {
         const char *e = std::getenv(n);
         r += e ? e : "-";
         r += ',';

@@ -1838,7 +1838,13 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
         const size_t static_smem = 2048 + sizeof(int) * kMaxEntries;   // barriers + offsets, rounded up
         const size_t pa_bytes = (size_t)kPieceA * R * kHeadDim * sizeof(float);
         const size_t pw_bytes = (size_t)R * std::max(1, tab.max_count) * 8;   // one round's (P, dS)
-        for (int pr = 1; pr <= 2; ++pr) {
+        // the fewest rounds per piece whose pieces fit in one wave (up to
+        // gwarps / 2: each round takes a phase-A and a phase-B warp); ViT-B
+        // shape, B = 256 (32 units in the last wave, four-round pieces):
+        // 182.2 -> 179.2 us against whole units
+        int max_pr = pl->gwarps / 2;
+        if (const char *e = getenv("FIBATT_BWD_PIECE_ROUNDS")) max_pr = std::max(1, std::min(max_pr, atoi(e)));
+        for (int pr = 1; pr <= max_pr; ++pr) {
             const int np = (rounds + pr - 1) / pr;
             // one-round pieces over kPieceA + kPieceB warps: the partial dQ
             // rows and the round's (P, dS) go to the unit scratch, which

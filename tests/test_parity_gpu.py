@@ -210,13 +210,13 @@ def test_resident_last_wave_pieces(split, snake, monkeypatch):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("pieces", ["0", "1", "1-serial"])
-@pytest.mark.parametrize("B", [13, 14, 27])
+@pytest.mark.parametrize("B", [13, 14, 15, 27])
 def test_resident_bwd_last_wave_pieces(B, pieces, dtype, monkeypatch):
-    # 156, 168 or 324 heads on (at most) 152 CTAs: the 4, 16 or 20 heads of
-    # the partial last wave are cut into pieces of one or two rounds, each
-    # piece recomputing P and dS for its key rows (B = 27: two full waves, the
-    # second in snake order); every gradient of every head compared with the
-    # oracle
+    # 156, 168, 180 or 324 heads on (at most) 152 CTAs: the 4, 16, 28 or 20
+    # heads of the partial last wave are cut into pieces of one, two or three
+    # rounds (fp32: more), each piece recomputing P and dS for its key rows
+    # (B = 27: two full waves, the second in snake order); every gradient of
+    # every head compared with the oracle
     # one-round pieces run spread over nine warps, or ("1-serial") on two
     monkeypatch.setenv("FIBATT_PATH", "resident")
     monkeypatch.setenv("FIBATT_BWD_PIECES", pieces[0])
