@@ -116,13 +116,11 @@ __device__ __forceinline__ void fused_row0(const uint8_t *sQ, const uint8_t *sK,
                     xb = fmaf(__uint_as_float(qv.y), __uint_as_float(kv.y), xb);
                     xa = fmaf(__uint_as_float(qv.z), __uint_as_float(kv.z), xa);
                     xb = fmaf(__uint_as_float(qv.w), __uint_as_float(kv.w), xb);
-                } else {
-                    const uint32_t q4[4] = {qv.x, qv.y, qv.z, qv.w}, k4[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        xa = fmaf(bf16_lo(q4[i]), bf16_lo(k4[i]), xa);
-                        xb = fmaf(bf16_hi(q4[i]), bf16_hi(k4[i]), xb);
-                    }
+                } else {   // mixed-precision FMAs on the packed pairs: no unpacking
+                    xa = dot2_bf16(qv.x, kv.x, xa);
+                    xb = dot2_bf16(qv.y, kv.y, xb);
+                    xa = dot2_bf16(qv.z, kv.z, xa);
+                    xb = dot2_bf16(qv.w, kv.w, xb);
                 }
             }
         }
