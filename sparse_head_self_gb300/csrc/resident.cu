@@ -1834,7 +1834,9 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
         int optin = 0;
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         const size_t static_smem = 2048 + sizeof(int) * kMaxEntries;   // barriers + offsets, rounded up
-        const size_t pa_bytes = (size_t)kPieceA * R * kHeadDim * sizeof(float);
+        // one-round pieces: the partial dQ rows of warps 1 .. kPieceA-1, then (if there is room) the
+        // round's (P, dS), in the unit scratch, which pieces use for nothing else
+        const size_t pa_bytes = (size_t)(kPieceA - 1) * R * kHeadDim * sizeof(float);
         const size_t pw_bytes = (size_t)R * std::max(1, tab.max_count) * 8;   // one round's (P, dS)
         // the fewest rounds per piece whose pieces fit in one wave (up to
         // gwarps / 2: each round takes a phase-A and a phase-B warp); ViT-B
@@ -1844,20 +1846,20 @@ bool plan_bwd_resident(const TableArg &tab, int B, fibatt_dtype dt, ResidentPlan
         if (const char *e = getenv("FIBATT_BWD_PIECE_ROUNDS")) max_pr = std::max(1, std::min(max_pr, atoi(e)));
         for (int pr = 1; pr <= max_pr; ++pr) {
             const int np = (rounds + pr - 1) / pr;
-            // one-round pieces over kPieceA + kPieceB warps: the partial dQ
-            // rows and the round's (P, dS) go to the unit scratch, which
-            // pieces use for nothing else
-            bool par = pr == 1 && pl->gwarps >= kPieceA + kPieceB && scratch >= pa_bytes + pw_bytes;
+            // one-round pieces over kPieceA + kPieceB warps
+            bool par = pr == 1 && pl->gwarps >= kPieceA + kPieceB && scratch >= pa_bytes;
             if (const char *e = getenv("FIBATT_BWD_PIECE_PAR")) par = par && atoi(e) != 0;
+            const bool pw_in_scratch = par && scratch >= pa_bytes + pw_bytes;
             // global token: one-round pieces only, with spare warps for the dense parts
             if (tab.global0 && !(par && pl->gwarps > kPieceA + kPieceB)) continue;
-            const size_t area = par ? 0 : (size_t)pr * R * std::max(1, tab.max_count) * 8;   // per phase-B warp
+            // the (P, dS) area of each phase-B warp, unless it went to the scratch
+            const size_t area = pw_in_scratch ? 0 : (size_t)pr * R * std::max(1, tab.max_count) * 8;
             if ((long)left * np <= pl->grid && 2 * pr <= pl->gwarps &&
                 pl->smem + area + static_smem <= (size_t)optin) {
                 pl->n_keep = units - left;
                 pl->qsub = np;
                 pl->sub_rows = pr;
-                pl->split_off = par ? stage * stages + pa_bytes : pl->smem;
+                pl->split_off = pw_in_scratch ? stage * stages + pa_bytes : pl->smem;
                 pl->smem += area;
                 pl->piece_par = par;
                 break;
