@@ -208,6 +208,17 @@ def test_resident_last_wave_pieces(split, snake, monkeypatch):
     _fwd_full(wl, seed=13)
 
 
+@pytest.mark.parametrize("gwarps", ["12", "11", "7"])
+@pytest.mark.parametrize("B", [13, 20])
+def test_resident_forward_rounds_circulate(gwarps, B, monkeypatch):
+    # fewer consumer warps than the 13 rounds of a 197-row head: the rounds
+    # circulate over the warps from unit to unit (B = 13: a last wave cut
+    # into pieces; B = 20: 240 whole-head units, two waves), every output
+    monkeypatch.setenv("FIBATT_PATH", "resident")
+    monkeypatch.setenv("FIBATT_FWD_GWARPS", gwarps)
+    _fwd_full(WORKLOADS["vitb"].with_batch(B), seed=31 + B)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("pieces", ["0", "1", "1-serial"])
 @pytest.mark.parametrize("B", [13, 14, 15, 27])
