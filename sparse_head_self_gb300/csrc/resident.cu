@@ -467,12 +467,12 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
     __shared__ int s_abort;                    // a bounded wait of this CTA gave up (mbar_wait)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0 && p.early_prefetch) {
+    if (threadIdx.x == 0 && (p.early_prefetch & 1)) {
         // Warm L2 with the first units' rows while the previous kernel drains.
         // A prefetch only moves lines into L2, the point of coherence: the
         // copies issued after the grid-dependency wait below still read what
         // the previous kernel wrote.
-        for (int i = 0; i < p.stages; ++i) {
+        for (int i = 0; i < ((p.early_prefetch & 2) ? 1 : p.stages); ++i) {
             const int u = fwd_slot_unit(p, i);
             if (u >= 0) prefetch_unit<T>(tab, p, u);
         }
@@ -512,6 +512,9 @@ fwd_pipe_kernel(const __grid_constant__ TableArg tab, const PipeParams p) {
                 }
             const Unit g = unit_geometry(tab, s_start, s_off, p, u);   // before the wait: off the critical path
             if (i >= p.stages && !mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1, &s_abort)) break;
+            // the second unit's copies wait for the first unit's rows to land, so
+            // that every CTA's first unit has the DRAM to itself at the start
+            if (i == 1 && (p.early_prefetch & 2) && !mbar_wait(&full_bar[0], 0, &s_abort)) break;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const size_t row0 = (size_t)g.bh * tab.N;
             uint32_t qb = (uint32_t)(g.q1 - g.q0) * RB, kvb = (uint32_t)g.nrows * RB;
@@ -1096,10 +1099,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
 
     const int N = tab.N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0 && p.early_prefetch) {
+    if (threadIdx.x == 0 && (p.early_prefetch & 1)) {
         // as in the forward: warm L2 with the first units' rows early
         const uint32_t b = (uint32_t)((size_t)N * RB);
-        for (int i = 0; i < p.stages; ++i) {
+        for (int i = 0; i < ((p.early_prefetch & 2) ? 1 : p.stages); ++i) {
             const int it = (int)blockIdx.x + i * (int)gridDim.x;
             if (it >= p.n_units) break;
             const size_t row0 = (size_t)bwd_item_unit(p, it) * N * kHeadDim;
@@ -1134,6 +1137,10 @@ bwd_pipe_kernel(const __grid_constant__ TableArg tab, const BwdParams p) {
             const int s = i % p.stages;
             // the lanes agree, so the warp leaves the loop together
             if (i >= p.stages && !__all_sync(kFullMask, mbar_wait(&empty_bar[s], ((i / p.stages) - 1) & 1, &s_abort)))
+                break;
+            // as in the forward: the second unit's copies wait for the first
+            // unit's rows to land
+            if (i == 1 && (p.early_prefetch & 2) && !__all_sync(kFullMask, mbar_wait(&full_bar[0], 0, &s_abort)))
                 break;
             uint8_t *st = smem + (size_t)s * p.stage_bytes;
             const bool fill_by_consumers = i == 0;
@@ -1575,12 +1582,22 @@ size_t row_bytes(fibatt_dtype dt) { return dt == FIBATT_F32 ? 256 : 128; }
 
 // Early L2 prefetch of each CTA's first units (FIBATT_EARLY_PREFETCH=0 turns
 // it off); it only pays with dependent launches.
-int early_prefetch() {
+// Bit 0: L2 prefetch of a CTA's first units before the grid-dependency wait
+// (FIBATT_EARLY_PREFETCH=0: off).  Bit 1: the first unit alone at the start,
+// its copies and prefetch issued before any other unit's (FIBATT_FIRST_ALONE:
+// 1, the default, for the forward; 2 for both kernels; 0 off).  Measured on
+// the ViT-B shape: forward 20.64 -> 20.57 us at B = 64, 19.28 -> 19.13 us
+// without the diagonal, 13.72 -> 13.21 us at B = 38; the backward 1-3%
+// slower (its producer's per-row pass for the second unit starts later).
+int early_prefetch(bool backward) {
     static const int on = [] {
         const char *e = getenv("FIBATT_EARLY_PREFETCH");
         return (e && atoi(e) == 0) ? 0 : 1;
     }();
-    return on && pdl_enabled();
+    const char *f = getenv("FIBATT_FIRST_ALONE");
+    const int mode = f ? atoi(f) : 1;
+    const bool alone = backward ? mode == 2 : mode >= 1;
+    return (on && pdl_enabled() ? 1 : 0) | (alone ? 2 : 0);
 }
 
 // Snake order of the forward's waves (FIBATT_FWD_SNAKE=0 turns it off; read
@@ -1760,7 +1777,7 @@ static cudaError_t fwd_resident(const FwdArgs &a, const ResidentPlan &pl) {
     const int n_reg = a.B * a.tab->H * pl.qsplit;
     PipeParams p{a.Q, a.K, a.V, a.O, a.LSE, a.scale * kLog2e, pl.qsplit, pl.chunk, pl.kv_cap,
                  pl.n_keep + (n_reg - pl.n_keep) * pl.qsub, pl.stages, pl.groups, pl.gwarps,
-                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows, early_prefetch(),
+                 (uint32_t)pl.stage_bytes, pl.prefetch, pl.n_keep, pl.qsub, pl.sub_rows, early_prefetch(false),
                  fwd_snake(), pl.fuse_row0};
     const cudaError_t e =
         launch_kernel(kern, dim3(pl.grid), dim3(pl.threads), pl.smem, a.stream, pdl_enabled(), *a.tab, p);
@@ -1917,7 +1934,7 @@ static cudaError_t bwd_resident(const BwdArgs &a, const ResidentPlan &pl, int un
     const int items = pl.n_keep + (units - pl.n_keep) * pl.qsub;
     BwdParams p{a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV, a.scale, a.scale * kLog2e,
                 items, pl.stages, pl.gwarps, (uint32_t)pl.stage_bytes,
-                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch(),
+                (uint32_t)(pl.stage_bytes * pl.stages), std::max(1, (int)a.tab->max_count), a.gw, early_prefetch(true),
                 pl.n_keep, pl.qsub, pl.sub_rows, (uint32_t)pl.split_off, bwd_snake(), pl.piece_par,
                 pl.fuse_row0, (uint32_t)pl.gt_off};
     const cudaError_t e =

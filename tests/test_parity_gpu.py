@@ -208,6 +208,19 @@ def test_resident_last_wave_pieces(split, snake, monkeypatch):
     _fwd_full(wl, seed=13)
 
 
+@pytest.mark.parametrize("mode", ["0", "1", "2"])
+@pytest.mark.parametrize("B", [13, 38])
+def test_resident_first_unit_alone(mode, B, monkeypatch):
+    # a CTA's second unit copied only after its first unit landed (1: the
+    # forward, the default; 2: both kernels; 0: neither), every output and
+    # gradient; B = 13: a last wave of pieces, B = 38: three whole waves
+    monkeypatch.setenv("FIBATT_PATH", "resident")
+    monkeypatch.setenv("FIBATT_FIRST_ALONE", mode)
+    wl = WORKLOADS["vitb"].with_batch(B)
+    _fwd_full(wl, seed=41 + B)
+    _bwd_full(wl, seed=41 + B)
+
+
 @pytest.mark.parametrize("gwarps", ["12", "11", "7"])
 @pytest.mark.parametrize("B", [13, 20])
 def test_resident_forward_rounds_circulate(gwarps, B, monkeypatch):
