@@ -205,9 +205,13 @@ const char *fibatt_version(void);
 
 /* Device-side error word of the current device: bit 0 (1) is set when a
  * kernel gave up waiting for its shared-memory staging copies (a bounded wait
- * of about 2 s; the kernel then returns without writing its outputs).  This
- * call synchronises with the device.  With clear != 0 the word is reset.
- * CUDA on a failed copy. */
+ * of about 2 s; the kernel then returns without writing its outputs); bit 1
+ * (2) when a producer left before its last copies had landed (also after
+ * about 2 s); bit 2 (4), in the bounds-checked debug build only (built with
+ * -DFIBATT_CHECKS), when a kernel's bounds check failed and it skipped the
+ * access (the first failing source line is then printed to stderr).  The
+ * word is the OR over every kernel file's copy.  This call synchronises with
+ * the device.  With clear != 0 the word is reset.  CUDA on a failed copy. */
 fibatt_status fibatt_device_error(int clear, unsigned *code);
 
 /* Number of CUDA kernels this library has launched in this process so far
