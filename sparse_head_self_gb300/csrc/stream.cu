@@ -618,7 +618,7 @@ __device__ __forceinline__ void dense_col_block(const TableArg &tab, const Strea
 }
 
 // The key rows [first, first + 32/G) of head bh (one warp; first < N).
-template <typename T, int G, bool GT>
+template <typename T, int G, bool GT, int KU = 1>
 __device__ __forceinline__ void key_rows(const TableArg &tab, const StreamParams &p, const int *s_off, int cnt, int bh,
                                          int first) {
     using S = Run<T, G>;
@@ -645,7 +645,34 @@ __device__ __forceinline__ void key_rows(const TableArg &tab, const StreamParams
     S kk, vv;
     kk.load(static_cast<const uint8_t *>(p.K) + (row0 + k) * RB + lo);
     vv.load(static_cast<const uint8_t *>(p.V) + (row0 + k) * RB + lo);
-    for (int t = tb; t < te; ++t) {
+    int t = tb;
+    if constexpr (KU == 2) {   // two entries per step: both pairs' row loads in flight together
+        for (; t + 1 < te; t += 2) {
+            const int j0 = k + s_off[t], j1 = k + s_off[t + 1];
+            const bool in0 = valid && (unsigned)j0 < (unsigned)N, in1 = valid && (unsigned)j1 < (unsigned)N;
+            const int c0 = in0 ? j0 : k, c1 = in1 ? j1 : k;
+            S q0, g0, q1, g1;
+            q0.load(gQ + (size_t)c0 * RB);
+            g0.load(gG + (size_t)c0 * RB);
+            q1.load(gQ + (size_t)c1 * RB);
+            g1.load(gG + (size_t)c1 * RB);
+            const float2 l0 = ld[c0], l1 = ld[c1];
+            const float s0 = lanes_sum<G>(q0.dot(kk)), dp0 = lanes_sum<G>(g0.dot(vv));
+            const float s1 = lanes_sum<G>(q1.dot(kk)), dp1 = lanes_sum<G>(g1.dot(vv));
+            const float P0 = in0 ? fast_exp2(fmaf(s0, sl2, -l0.x)) : 0.f;
+            const float P1 = in1 ? fast_exp2(fmaf(s1, sl2, -l1.x)) : 0.f;
+            const float dS0 = P0 * (dp0 - l0.y), dS1 = P1 * (dp1 - l1.y);
+            g0.axpy(P0, dv);
+            q0.axpy(dS0, dk);
+            g1.axpy(P1, dv);
+            q1.axpy(dS1, dk);
+            if (in0 && sub == 0 && FIBATT_CHECKED(t < cnt && cnt <= p.max_count && j0 < p.ns))
+                scr[(ptrdiff_t)j0 - (ptrdiff_t)t * p.ns] = dS0;
+            if (in1 && sub == 0 && FIBATT_CHECKED(t + 1 < cnt && cnt <= p.max_count && j1 < p.ns))
+                scr[(ptrdiff_t)j1 - (ptrdiff_t)(t + 1) * p.ns] = dS1;
+        }
+    }
+    for (; t < te; ++t) {
         const int j = k + s_off[t];
         const bool in = valid && (unsigned)j < (unsigned)N;
         const int jc = in ? j : k;   // any row in range: its pair is masked
@@ -687,8 +714,8 @@ __device__ __forceinline__ void key_rows(const TableArg &tab, const StreamParams
 
 // Key-centric pass: key row k stationary; the queries attending it are
 // j = k + off[t] (symmetric table), whose pair is query j's entry cnt-1-t.
-template <typename T, int G, int W, bool GT>
-__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? ((GT ? 20 : 24) / W > 0 ? (GT ? 20 : 24) / W : 1) : 1)
+template <typename T, int G, int W, bool GT, int KU = 1>
+__global__ void __launch_bounds__(W * 32, (G == 4 && sizeof(T) == 2) ? ((GT || KU == 2 ? 20 : 24) / W > 0 ? (GT || KU == 2 ? 20 : 24) / W : 1) : 1)
 bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p) {
     using S = Run<T, G>;
     constexpr int R = 32 / G;
@@ -719,7 +746,7 @@ bwd_key_stream_kernel(const __grid_constant__ TableArg tab, const StreamParams p
     grid_dep_wait();
     grid_dep_launch();
     const int first = (yb * W + (int)(threadIdx.x >> 5)) * R;
-    if (first < N) key_rows<T, G, GT>(tab, p, s_off, cnt, bh, first);   // whole warps
+    if (first < N) key_rows<T, G, GT, KU>(tab, p, s_off, cnt, bh, first);   // whole warps
 }
 
 // Query-centric pass: dQ_j = scale sum over in-range entries t of
@@ -837,6 +864,16 @@ int stream_lanes() {
 int stream_prefetch() {
     const char *e = getenv("FIBATT_STREAM_PREFETCH");
     return e ? atoi(e) & 7 : 4;
+}
+
+// Table entries per step of the key pass (FIBATT_KEY_UNROLL: 2, the
+// default for bf16 rows, four lanes, four warps, no global token; 1).  Two entries keep both
+// pairs' query and dO rows in flight together, at 96 registers (20 warps per
+// SM against 24): video backward 95.0 -> 93.2 us, 128 x 128 image 413.4 ->
+// 406.0 us.
+int key_unroll() {
+    const char *e = getenv("FIBATT_KEY_UNROLL");
+    return e && atoi(e) == 1 ? 1 : 2;
 }
 
 bool stream_w16() {
@@ -983,8 +1020,17 @@ cudaError_t bwd_stream(const BwdArgs &a) {
     if (e == cudaSuccess) e = cudaGetLastError();
     p.Out = a.dQ;   // the key pass's dense dQ_0 blocks write row 0 of dQ
     if (e == cudaSuccess)
-        e = launch_kernel(bwd_key_stream_kernel<T, G, W, GT>, dim3(blocks + 2 * (unsigned)p.row0_heads), block, smem,
-                          a.stream, pdl, tab, p);
+        e = [&] {
+            // the default shape without the global token (with it, whose key pass already runs at 96
+            // registers, two entries per step measured slower: 128 x 128 image 524.0 -> 541.3 us)
+            if constexpr (sizeof(T) == 2 && G == 4 && W == kStreamWarps && !GT) {
+                if (key_unroll() == 2)
+                    return launch_kernel(bwd_key_stream_kernel<T, G, W, GT, 2>,
+                                         dim3(blocks + 2 * (unsigned)p.row0_heads), block, smem, a.stream, pdl, tab, p);
+            }
+            return launch_kernel(bwd_key_stream_kernel<T, G, W, GT>, dim3(blocks + 2 * (unsigned)p.row0_heads), block,
+                                 smem, a.stream, pdl, tab, p);
+        }();
     if (e == cudaSuccess) e = cudaGetLastError();
     p.Out = a.dQ;
     if (e == cudaSuccess)

@@ -89,6 +89,26 @@ def test_video_shape_one_batch_fwd_full():
     _fwd_full(wl, seed=7)
 
 
+@pytest.mark.parametrize("key_unroll", ["1", "2"])
+def test_video_shape_two_heads_bwd_key_pass_steps(key_unroll, monkeypatch):
+    # the streaming key pass with one or two table entries per step (ragged
+    # tails of odd entry counts included: heads with 13 and 19 entries)
+    monkeypatch.setenv("FIBATT_PATH", "flat")
+    monkeypatch.setenv("FIBATT_KEY_UNROLL", key_unroll)
+    wl = WORKLOADS["video"].with_batch(1)
+    q, k, v, do = make_inputs(wl, 10)
+    sup = support_for(wl)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    O, L = api.fwd(sup, qd, kd, vd, wl.scale)
+    dQ, dK, dV = api.bwd(sup, qd, kd, vd, O, L, dod, wl.scale)
+    heads = oracle_heads(wl)
+    for h in (0, 1, wl.H - 1):
+        rQ, rK, rV = oracle.bwd_head(q[0, h], k[0, h], v[0, h], do[0, h], heads[h], wl.scale)
+        assert_close(f"video h{h} dQ", dQ[0, h].float().cpu(), rQ, wl.dtype)
+        assert_close(f"video h{h} dK", dK[0, h].float().cpu(), rK, wl.dtype)
+        assert_close(f"video h{h} dV", dV[0, h].float().cpu(), rV, wl.dtype)
+
+
 @pytest.mark.parametrize("kernel_path", ["generic", "flat", "flat_window", "flat_legacy"], indirect=True)
 def test_video_shape_two_heads_bwd_full(kernel_path):
     # every row of two heads (the narrowest and the widest window) of one
